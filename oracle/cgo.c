@@ -153,9 +153,11 @@ static uint32_t ceil_div(uint32_t a, uint32_t b) { return (a + b - 1u) / b; }
 typedef struct {
     uint32_t n_chunks;
     uint32_t anchors_per_full_chunk;
+    uint32_t spans_full;     /* spans in a full chunk */
     uint32_t A;              /* anchor rows in total */
     uint32_t spans_total;    /* spans over all chunks */
     uint32_t NG;             /* channel groups */
+    uint32_t n_slices;       /* L * 2 */
     uint64_t n_streams;
     uint64_t n_tables;
 } geom;
@@ -183,6 +185,8 @@ static void make_geom(const cgo_config *cfg, geom *g)
 {
     g->n_chunks = ceil_div(cfg->T, cfg->chunk_tokens);
     g->anchors_per_full_chunk = ceil_div(cfg->chunk_tokens, cfg->G);
+    g->spans_full = ceil_div(cfg->chunk_tokens, cfg->tokens_per_stream);
+    g->n_slices = cfg->L * 2u;
     g->A = 0;
     g->spans_total = 0;
     for (uint32_t ch = 0; ch < g->n_chunks; ch++) {
@@ -199,11 +203,33 @@ static void make_geom(const cgo_config *cfg, geom *g)
 static uint32_t pos_in_chunk(const cgo_config *cfg, uint32_t t) { return t % cfg->chunk_tokens; }
 static int is_anchor(const cgo_config *cfg, uint32_t t) { return pos_in_chunk(cfg, t) % cfg->G == 0; }
 
-/* Row of the anchor plane holding the anchor of token t's group (R7). */
+/* Row, among one slice's anchor rows in token order, of the anchor of token
+ * t's group (R7: groups restart at every chunk). */
 static uint32_t anchor_row(const cgo_config *cfg, const geom *g, uint32_t t)
 {
     uint32_t ch = t / cfg->chunk_tokens;
     return ch * g->anchors_per_full_chunk + pos_in_chunk(cfg, t) / cfg->G;
+}
+
+/* The object keeps everything chunk-major so that one chunk is one
+ * contiguous range of every per-chunk section.  Anchor plane:
+ * [chunk][L*2 slices][anchor rows of the chunk][C]; this is the index of
+ * (slice, anchor of token t, channel 0). */
+static uint64_t anchor_index(const cgo_config *cfg, const geom *g, uint32_t slice, uint32_t t)
+{
+    uint32_t ch = t / cfg->chunk_tokens;
+    uint32_t apc = ceil_div(chunk_len(cfg, ch), cfg->G);
+    uint64_t row = (uint64_t)ch * g->anchors_per_full_chunk * g->n_slices + (uint64_t)slice * apc +
+                   pos_in_chunk(cfg, t) / cfg->G;
+    return row * cfg->C;
+}
+
+/* Streams are ordered (chunk, slice, span in chunk, channel group). */
+static uint64_t stream_index(const cgo_config *cfg, const geom *g, uint32_t ch, uint32_t slice, uint32_t span,
+                             uint32_t gi)
+{
+    uint32_t spc = ceil_div(chunk_len(cfg, ch), cfg->tokens_per_stream);
+    return (((uint64_t)ch * g->spans_full * g->n_slices + (uint64_t)slice * spc + span) * g->NG) + gi;
 }
 
 /* Worst-case sizes: out[0]=A, [1]=spans_total, [2]=n_streams, [3]=n_tables,
@@ -624,7 +650,7 @@ static int slice_decode(const cgo_config *cfg, const geom *g, uint32_t l, const 
     const uint32_t T = cfg->T, C = cfg->C;
     const float step = cfg->step[l];
     const float *scales = in->scales + slice * C;
-    const int8_t *anch = in->anchors + slice * (uint64_t)g->A * C;
+    const int8_t *anch = in->anchors;
     uint32_t *freq = calloc((size_t)C * 256u, sizeof(uint32_t));
     int32_t *lo = malloc(sizeof(int32_t) * C), *hi = malloc(sizeof(int32_t) * C);
     uint32_t *tok = malloc(sizeof(uint32_t) * cfg->tokens_per_stream);
@@ -671,18 +697,18 @@ static int slice_decode(const cgo_config *cfg, const geom *g, uint32_t l, const 
     /* anchors */
     for (uint32_t t = 0; t < T; t++) {
         if (!is_anchor(cfg, t)) continue;
-        uint32_t row = anchor_row(cfg, g, t);
+        uint64_t ai = anchor_index(cfg, g, (uint32_t)slice, t);
         for (uint32_t c = 0; c < C; c++)
-            y[(size_t)t * C + c] = cgo_f32_to_f16((float)anch[(size_t)row * C + c] * scales[c]);
+            y[(size_t)t * C + c] = cgo_f32_to_f16((float)anch[ai + c] * scales[c]);
     }
     /* streams */
-    uint64_t k = slice * (uint64_t)g->spans_total * g->NG;
     for (uint32_t ch = 0; ch < g->n_chunks; ch++) {
         uint32_t c0 = ch * cfg->chunk_tokens, len = chunk_len(cfg, ch);
         for (uint32_t s0 = 0; s0 < len; s0 += cfg->tokens_per_stream) {
             uint32_t s1 = s0 + cfg->tokens_per_stream < len ? s0 + cfg->tokens_per_stream : len;
             uint32_t nst = span_steps(cfg, c0 + s0, c0 + s1, tok);
-            for (uint32_t gi = 0; gi < g->NG; gi++, k++) {
+            for (uint32_t gi = 0; gi < g->NG; gi++) {
+                uint64_t k = stream_index(cfg, g, ch, (uint32_t)slice, s0 / cfg->tokens_per_stream, gi);
                 uint64_t b = in->stream_off[k], e = in->stream_off[k + 1];
                 if (e < b || (b & 15u) || (e & 15u) || e > in->payload_cap) {
                     st = CGO_ERR_CORRUPT;
@@ -713,7 +739,8 @@ static int slice_decode(const cgo_config *cfg, const geom *g, uint32_t l, const 
                     goto done;
                 }
                 for (uint32_t j = 0; j < nst; j++) {
-                    uint32_t t = tok[j], row = anchor_row(cfg, g, t);
+                    uint32_t t = tok[j];
+                    uint64_t ai = anchor_index(cfg, g, (uint32_t)slice, t);
                     for (uint32_t i = 0; i < CGO_LANES; i++) {
                         uint32_t c = gi * CGO_LANES + i, s = sym[(size_t)j * CGO_LANES + i];
                         int32_t qv;
@@ -726,7 +753,7 @@ static int slice_decode(const cgo_config *cfg, const geom *g, uint32_t l, const 
                         } else {
                             qv = (int32_t)s - 127;
                         }
-                        float xa = (float)anch[(size_t)row * C + c] * scales[c];
+                        float xa = (float)anch[ai + c] * scales[c];
                         float dq = (float)qv * step;
                         y[(size_t)t * C + c] = cgo_f32_to_f16(xa + dq);
                     }
@@ -824,14 +851,16 @@ static int run_threads(work *proto, void *(*fn)(void *), int nthreads)
 }
 
 /*
- * Encode a whole cache kv [L][2][T][C] (fp16 bits).  Layout of the object:
- *   anchors    int8  [L][2][A][C]
+ * Encode a whole cache kv [L][2][T][C] (fp16 bits).  Layout of the object
+ * (per-chunk sections are chunk-major, so one chunk is one contiguous range
+ * of each of them):
+ *   anchors    int8  [chunk][L][2][anchor rows of the chunk][C]
  *   scales     fp32  [L][2][C]
  *   tables     per (l, kv, c) in that order: u8 lo, u8 hi, then the 16-bit
  *              little-endian values f_s - 1 for s = lo..hi; an empty table is
  *              lo = 1, hi = 0 (2 bytes)
  *   table_off  u32   [L*2*C + 1] byte offsets of the tables
- *   payload    streams ordered by (l, kv, chunk, span, group); a stream is
+ *   payload    streams ordered by (chunk, l, kv, span, group); a stream is
  *              its 16-bit words followed by zero words up to a multiple of 8
  *   stream_off u64   [n_streams + 1] byte offsets (multiples of 16)
  *   escapes    int32 escaped q values, per stream in (step, lane) order
@@ -850,35 +879,66 @@ int cgo_encode(const cgo_config *cfg, const uint16_t *kv, cgo_encoded *out, cgo_
     work w = {cfg, &g, kv, NULL, NULL, sl, n_slices, 1, 0, 0};
     st = run_threads(&w, enc_worker, nthreads);
     if (st) goto done;
-    /* global offsets and copies */
+    /* global offsets and copies: tables and scales slice by slice, then the
+     * per-chunk sections chunk-major */
     uint64_t toff = 0, poff = 0, eoff = 0, k = 0;
     const uint64_t n_sl_str = (uint64_t)g.spans_total * g.NG;
+    uint64_t *wpre = malloc(sizeof(uint64_t) * (n_sl_str + 1) * n_slices);
+    uint64_t *epre = malloc(sizeof(uint64_t) * (n_sl_str + 1) * n_slices);
+    if (!wpre || !epre) {
+        free(wpre);
+        free(epre);
+        st = CGO_ERR_NOMEM;
+        goto done;
+    }
     for (uint32_t s = 0; s < n_slices; s++) {
         slice_enc *e = &sl[s];
         memcpy(out->scales + (uint64_t)s * cfg->C, e->scales, sizeof(float) * cfg->C);
-        memcpy(out->anchors + (uint64_t)s * g.A * cfg->C, e->anchors, (size_t)g.A * cfg->C);
         if (toff + e->tables_bytes > out->tables_cap) {
             st = CGO_ERR_RANGE;
-            goto done;
+            break;
         }
         memcpy(out->tables + toff, e->tables, e->tables_bytes);
         for (uint32_t c = 0; c < cfg->C; c++) {
             out->table_off[(uint64_t)s * cfg->C + c] = (uint32_t)toff;
             toff += e->table_size[c];
         }
-        if (poff + 2u * e->n_words > out->payload_cap || eoff + e->n_esc > out->escapes_cap) {
-            st = CGO_ERR_RANGE;
-            goto done;
-        }
-        memcpy(out->payload + poff, e->words, 2u * e->n_words);
-        memcpy(out->escapes + eoff, e->esc, sizeof(int32_t) * e->n_esc);
-        for (uint64_t j = 0; j < n_sl_str; j++, k++) {
-            out->stream_off[k] = poff;
-            out->esc_off[k] = (uint32_t)eoff;
-            poff += 2u * e->stream_words[j];
-            eoff += e->stream_esc[j];
+        uint64_t *wp = wpre + (uint64_t)s * (n_sl_str + 1), *ep = epre + (uint64_t)s * (n_sl_str + 1);
+        wp[0] = ep[0] = 0;
+        for (uint64_t j = 0; j < n_sl_str; j++) {
+            wp[j + 1] = wp[j] + e->stream_words[j];
+            ep[j + 1] = ep[j] + e->stream_esc[j];
         }
     }
+    uint64_t arow = 0;
+    for (uint32_t ch = 0; ch < g.n_chunks && !st; ch++) {
+        uint32_t len = chunk_len(cfg, ch);
+        uint32_t apc = ceil_div(len, cfg->G), spc = ceil_div(len, cfg->tokens_per_stream);
+        for (uint32_t s = 0; s < n_slices && !st; s++) {
+            slice_enc *e = &sl[s];
+            memcpy(out->anchors + arow * cfg->C, e->anchors + (uint64_t)ch * g.anchors_per_full_chunk * cfg->C,
+                   (size_t)apc * cfg->C);
+            arow += apc;
+            const uint64_t *wp = wpre + (uint64_t)s * (n_sl_str + 1), *ep = epre + (uint64_t)s * (n_sl_str + 1);
+            uint64_t j0 = (uint64_t)ch * g.spans_full * g.NG, j1 = j0 + (uint64_t)spc * g.NG;
+            for (uint64_t j = j0; j < j1; j++, k++) {
+                uint64_t nb = 2u * e->stream_words[j], ne = e->stream_esc[j];
+                if (poff + nb > out->payload_cap || eoff + ne > out->escapes_cap) {
+                    st = CGO_ERR_RANGE;
+                    break;
+                }
+                out->stream_off[k] = poff;
+                out->esc_off[k] = (uint32_t)eoff;
+                memcpy(out->payload + poff, e->words + wp[j], nb);
+                memcpy(out->escapes + eoff, e->esc + ep[j], sizeof(int32_t) * ne);
+                poff += nb;
+                eoff += ne;
+            }
+        }
+    }
+    free(wpre);
+    free(epre);
+    if (st) goto done;
     out->table_off[g.n_tables] = (uint32_t)toff;
     out->stream_off[g.n_streams] = poff;
     out->esc_off[g.n_streams] = (uint32_t)eoff;
@@ -920,7 +980,8 @@ int cgo_anchor_scales(const cgo_config *cfg, const uint16_t *kv, float *scales)
     return CGO_OK;
 }
 
-/* E2 + E3 for a whole cache: anchors [L][2][A][C], q [L][2][T][C]. */
+/* E2 + E3 for a whole cache: anchors [L][2][A][C] (each slice's anchor rows
+ * in token order, not the object's chunk-major plane), q [L][2][T][C]. */
 int cgo_quantize(const cgo_config *cfg, const uint16_t *kv, const float *scales, int8_t *anchors, int32_t *q)
 {
     int st = check_config(cfg);
