@@ -1,0 +1,309 @@
+"""Benchmark of the KV-cache codec hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over a seeded synthetic
+Llama-70B-shaped KV cache (80 layers x {K,V} x 16384 tokens x 8x128 fp16,
+5.4 GB): cg_encode (anchor scale/quantize, layer-binned delta quantization,
+histograms, 16-bit tables, interleaved range-ANS encode, prefix-sum pack)
+then cg_decode of the result.  `value` is fp16 KV GB/s over the whole step;
+the decode and encode phases are also reported on their own (CUDA events on
+the launching stream).  Inputs (5.4 GB) are larger than L2, so no flush is
+needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (the plain C implementation the
+parity tests use) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "cg_decode / cg_encode GB/s of fp16 KV (1xGB300, % HBM roofline); bits/value"
+UNIT = "GB/s"
+KERNELS_PER_STEP = 8  # k_stats, 3 x k_scan, k_encode, k_pack, k_sizes, k_decode_all
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class Clocks:
+    """Samples nvidia-smi every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in self.rows if num(r[1])]
+        mx = [num(r[2]) for r in self.rows if num(r[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in self.rows)}
+
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, rank, ws, local
+    return None, 0, 1, local
+
+
+def max_over_ranks(dist, v: float, device) -> float:
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device):
+    if dist is not None:
+        dist.barrier(device_ids=[device.index]) if device.type == "cuda" else dist.barrier()
+
+
+def cpu_baseline(workload, seconds_hint=20.0):
+    """The oracle as it stands, on a bounded sample: encode + decode of the
+    first layer of the workload (one chunk layout, all host threads)."""
+    from oracle import oracle as O
+    from kv_cache_compression_decode_gb300 import synth
+
+    cores = os.cpu_count() or 1
+    L1 = 1
+    x = synth.ar1_kv(L1, workload.T, workload.C, workload.rho, workload.n_outlier, workload.seed).numpy()
+    oc = O.Config(L1, workload.T, workload.C, 10, workload.chunk, workload.tokens_per_stream,
+                  O.layer_steps(workload.L)[:L1])
+    x16 = x.view(np.uint16)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        enc = O.encode(oc, x16, nthreads=cores)
+        O.decode(oc, enc, nthreads=cores)
+        reps += 1
+        if time.perf_counter() - t0 > min(seconds_hint, 30.0) or reps >= 20:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    gbs = x16.nbytes / dt / 1e9
+    return {"value": gbs, "unit": UNIT, "cores": min(cores, 2 * L1), "kind": "oracle",
+            "sample": f"encode+decode of layer 0 (2 slices, {workload.T} tokens x {workload.C} channels, "
+                      f"{x16.nbytes / 1e6:.0f} MB fp16) of {workload.name}, {reps} reps, threads over (layer, K/V) "
+                      f"slices"}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle on a bounded sample, same metric."""
+    from kv_cache_compression_decode_gb300 import synth
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = synth.LLAMA70B
+    base = cpu_baseline(w, seconds_hint=max(5.0, 60.0 / max(1, args.steps + args.warmup)))
+    line = {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "data": "synthetic",
+            "dtype": "f32", "config": {"workload": w.name, "sample": base["sample"]},
+            "cpu_baseline": base,
+            "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    from kv_cache_compression_decode_gb300 import codec as C
+    from kv_cache_compression_decode_gb300 import synth
+
+    dist, rank, world, local = dist_init()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.LLAMA70B
+    cfg = C.Config(w.L, w.T, w.C, w.group_size, w.chunk, w.tokens_per_stream, C.layer_steps(w.L))
+    kv = w.generate(device=dev)
+    enc = C.Encoder(cfg, dev)
+    out = torch.empty_like(kv)
+    dstatus = C.new_status(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        enc.launch(kv, stream)
+        if ev:
+            ev[1].record(stream)
+        C.cg_decode(cfg, enc.out, out, dstatus, stream)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    st = C.read_status(enc.status) or C.read_status(dstatus)
+    if st != C.CG_OK:
+        raise C.CodecError(st, "warm-up step")
+    sizes = enc.result().sizes
+    comp_bytes = sizes["total_bytes"]
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with Clocks(dev.index) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    total_ms = max_over_ranks(dist, t_start.elapsed_time(t_end), dev)
+    enc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    st = C.read_status(enc.status) or C.read_status(dstatus)
+    if st != C.CG_OK:
+        raise C.CodecError(st, "timed steps")
+
+    fp16 = w.fp16_bytes
+    ms_per_step = total_ms / args.steps
+    value = world * fp16 / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    dec_alg = fp16 + comp_bytes  # compressed in + fp16 out per decode launch
+    dec_achieved = dec_alg / (dec_ms * 1e-3) / 1e9
+    enc_alg = fp16 + comp_bytes
+    enc_achieved = enc_alg / (enc_ms * 1e-3) / 1e9
+
+    # end to end through the C ABI with host buffers: pinned fp16 cache in,
+    # encode + decode, the sizes (bits/value) read back, every step
+    e2e = None
+    if not args.no_e2e:
+        host_kv = torch.empty(kv.shape, dtype=kv.dtype, pin_memory=True)
+        host_kv.copy_(kv)
+        kv_dev = torch.empty_like(kv)
+        for i in range(2):
+            kv_dev.copy_(host_kv, non_blocking=True)
+            step()
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n_e2e = max(2, min(args.steps, 5))
+        for i in range(n_e2e):
+            kv_dev.copy_(host_kv, non_blocking=True)
+            enc.launch(kv_dev, stream)
+            C.cg_decode(cfg, enc.out, out, dstatus, stream)  # cg_encode reads its sizes back (32 B D2H)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1), dev) / n_e2e
+        e2e = {"value": world * fp16 / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": fp16,
+               "d2h_bytes_per_step": 32, "ms_per_step": e2e_ms}
+        del host_kv, kv_dev
+
+    base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        base = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32+u32", "data": "synthetic",
+            "config": {"workload": w.name, "L": w.L, "T": w.T, "C": w.C, "group_size": w.group_size,
+                       "tokens_per_stream": w.tokens_per_stream, "steps_per_layer_third": [0.5, 1.0, 1.5],
+                       "fp16_bytes": fp16, "step": "cg_encode + cg_decode of the whole cache",
+                       "l2": "inputs (5.4 GB) larger than L2; no flush", "parallelism": f"replicas x{world}"},
+            "decode": {"gbs_fp16": round(fp16 / (dec_ms * 1e-3) / 1e9, 2), "ms": round(dec_ms, 4),
+                       "hbm_frac": round(dec_achieved / peak, 4)},
+            "encode": {"gbs_fp16": round(fp16 / (enc_ms * 1e-3) / 1e9, 2), "ms": round(enc_ms, 4),
+                       "hbm_frac": round(enc_achieved / peak, 4)},
+            "bits_per_value": round(8 * comp_bytes / w.values, 4),
+            "payload_bits_per_value": round(8 * sizes["payload_bytes"] / w.values, 4),
+            "compressed_bytes": comp_bytes,
+            "roofline": {"bound": "hbm", "kernel": "k_decode_all", "achieved": round(dec_achieved, 1),
+                         "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "unit": "GB/s",
+                         "frac": round(dec_achieved / peak, 4), "traffic": None,
+                         "algorithmic_bytes": dec_alg},
+            "encode_roofline": {"bound": "hbm", "achieved": round(enc_achieved, 1), "peak": peak, "unit": "GB/s",
+                                "frac": round(enc_achieved / peak, 4)},
+            "cpu_baseline": base,
+            "e2e": e2e,
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,232 @@
+/*
+ * cg.h -- C ABI of the GB300 KV-cache codec (CacheGen-style tensor codec).
+ *
+ * The codec turns a fp16 KV cache kv[L][2][T][C] (layers x {K,V} x tokens x
+ * heads*head_dim) into a compact bitstream and back.  It follows the method
+ * the CacheGen pages describe:
+ *   - tokens are cut into groups of `group_size` (10); the first token of a
+ *     group is the anchor, kept at 8 bits, and the other tokens are coded as
+ *     deltas against it ("CacheGen vs 传统量化KV缓存压缩技术深度对比与性能测试",
+ *     §2.1, compression pipeline stage 1);
+ *   - deltas are quantized with a per-layer step, finer for shallow layers
+ *     (0.5 / 1.0 / 1.5 for the layer thirds; same page, §1 and §2.1 stage 2);
+ *   - the symbols are arithmetic-coded with separate statistics per (layer,
+ *     channel) (same page, §1; "CacheGen: KV Cache Compression and Streaming
+ *     for Fast Large Language Model Serving", sciencestack page, TL;DR and
+ *     Figure 5), here a 32-bit range-ANS coder with 16-bit tables;
+ *   - long contexts are cut into ~1.5K-token chunks that decode on their own
+ *     and can each be stored at several quality levels (same page, §2.2);
+ *   - decoding runs on the GPU and can be pipelined with the transfer of the
+ *     compressed chunks (gptget.net page on the same paper, method details).
+ *
+ * Conventions for every entry point:
+ *   - The library allocates nothing and keeps no global state.  Every buffer
+ *     is owned by the caller.  "device" pointers are CUDA device memory of
+ *     the current device, "host" pointers are CPU memory.
+ *   - GPU work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous: outputs are valid after the stream is
+ *     synchronized.
+ *   - A status returned by the call itself means nothing was enqueued
+ *     (CG_ERR_INVALID_ARG, CG_ERR_RANGE for a buffer found too small on the
+ *     host) or a launch failed (CG_ERR_CUDA).
+ *   - Data-dependent errors found on the GPU are OR-ed into `*dev_status`
+ *     (a device uint32_t the caller clears beforehand) as the bit
+ *     (1u << code): CG_ERR_NONFINITE, CG_ERR_RANGE, CG_ERR_CORRUPT,
+ *     CG_ERR_TIMEOUT.  Read it after synchronizing; cg_status_from_flags()
+ *     turns it into a status.  Outputs are undefined when it is non-zero.
+ *   - fp16 tensors are passed as their 16-bit patterns (uint16_t).
+ *
+ * Encoded object (all sections little-endian; per-chunk sections are
+ * chunk-major so one chunk is one contiguous range of each):
+ *   anchors    int8   [n_chunks][L][2][anchor rows of the chunk][C]
+ *   scales     float  [L][2][C]          anchor scale per (layer, K/V, channel)
+ *   tables     bytes  per (l, kv, c) in that order: u8 lo, u8 hi, then u16
+ *                     (f_s - 1) for s = lo..hi; an empty table is lo=1, hi=0
+ *   table_off  u32    [L*2*C + 1]        byte offsets into `tables`
+ *   payload    bytes  streams ordered (chunk, l, kv, span, channel group);
+ *                     a stream is its u16 words then zero words up to a
+ *                     multiple of 8 words (16 bytes)
+ *   stream_off u64    [n_streams + 1]    byte offsets into `payload` (x16)
+ *   escapes    int32  quantized deltas outside [-127, 127], per stream in
+ *                     (step, lane) order
+ *   esc_off    u32    [n_streams + 1]    indices into `escapes`
+ */
+#ifndef CG_H
+#define CG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CG_OK = 0,
+    CG_ERR_INVALID_ARG = 1, /* bad configuration, pointer or size; nothing enqueued */
+    CG_ERR_NONFINITE = 2,   /* the input cache holds NaN or Inf */
+    CG_ERR_RANGE = 3,       /* an output or workspace buffer is too small */
+    CG_ERR_CORRUPT = 4,     /* an encoded object failed its integrity checks */
+    CG_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up */
+    CG_ERR_CUDA = 6         /* a CUDA call or kernel launch failed */
+} cg_status;
+
+/* Codec configuration.  Checked on the host by every call:
+ *   L >= 1, L <= CG_MAX_LAYERS; T >= 1; C >= 32 and C % 32 == 0;
+ *   group_size >= 1; chunk_tokens >= 1 (groups restart at every chunk);
+ *   tokens_per_stream >= 1 (a stream covers at most this many tokens of one
+ *   chunk); step: host array of L floats, each finite and > 2^-10. */
+#define CG_MAX_LAYERS 1024u
+typedef struct {
+    uint32_t L, T, C, group_size, chunk_tokens, tokens_per_stream;
+    const float *step; /* host, L entries: quantization step per layer */
+} cg_config;
+
+/* Sizes derived from a configuration (cg_encode_bounds). */
+typedef struct {
+    uint64_t A;                 /* anchor rows per (layer, K/V) */
+    uint64_t n_chunks, spans_total, n_streams, n_tables;
+    uint64_t anchors_bytes;     /* int8 anchor plane */
+    uint64_t scales_bytes;      /* float scales */
+    uint64_t table_off_bytes;   /* u32 [n_tables + 1] */
+    uint64_t tables_max_bytes;  /* worst-case compact tables */
+    uint64_t stream_off_bytes;  /* u64 [n_streams + 1] */
+    uint64_t payload_max_bytes; /* worst-case payload */
+    uint64_t esc_off_bytes;     /* u32 [n_streams + 1] */
+    uint64_t escapes_max_count; /* worst-case escapes (every delta) */
+    uint64_t workspace_bytes;   /* device workspace cg_encode needs */
+} cg_bounds;
+
+/* An encoded object.  For cg_encode these are device pointers to
+ * caller-allocated outputs with the given capacities; for cg_decode they
+ * point to a complete object in device memory; for cg_serialize /
+ * cg_deserialize they point to host memory. */
+typedef struct {
+    int8_t *anchors;
+    float *scales;
+    uint8_t *tables;
+    uint32_t *table_off;
+    uint8_t *payload;
+    uint64_t *stream_off;
+    int32_t *escapes;
+    uint32_t *esc_off;
+    uint64_t tables_cap;  /* bytes available at `tables` */
+    uint64_t payload_cap; /* bytes available at `payload` */
+    uint64_t escapes_cap; /* int32 entries available at `escapes` */
+} cg_encoded;
+
+/* Actual sizes of an encoded object. */
+typedef struct {
+    uint64_t payload_bytes, tables_bytes, n_escapes, total_bytes;
+} cg_sizes;
+
+/* Text for a status code.  Never NULL. */
+const char *cg_status_string(cg_status s);
+
+/* First error code set in a device status word (CG_OK when zero). */
+cg_status cg_status_from_flags(uint32_t flags);
+
+/* Fill *b with the sizes of every section and of the encode workspace for
+ * `cfg`.  Host only; no CUDA call.  CG_ERR_INVALID_ARG on a bad config,
+ * CG_ERR_RANGE if an offset section would overflow its integer type. */
+cg_status cg_encode_bounds(const cg_config *cfg, cg_bounds *b);
+
+/*
+ * Encode kv (device, fp16 bits, [L][2][T][C] contiguous) into `out`.
+ * Implements the whole encoder: anchor scale and int8 anchors, delta
+ * quantization with the layer's step (escape symbol 255 for |q| > 127),
+ * per-(layer, K/V, channel) histograms normalized to 16-bit frequency tables,
+ * interleaved range-ANS coding of every stream, and the prefix-sum pack of
+ * the streams into one payload (the compression pipeline of
+ * "CacheGen vs 传统量化KV缓存压缩技术深度对比与性能测试", §2.1).
+ *   ws, ws_bytes: device workspace, at least cg_bounds.workspace_bytes,
+ *                 256-byte aligned; contents on entry do not matter.
+ *   out:          host struct of device pointers; anchors, scales, table_off,
+ *                 stream_off and esc_off must hold their full sections,
+ *                 tables/payload/escapes at least *_cap bytes/entries.
+ *   sizes:        host memory (pinned for a truly asynchronous call) that
+ *                 receives the actual sizes once the stream has completed.
+ *   dev_status:   device word; NONFINITE on NaN/Inf input, RANGE when a
+ *                 capacity in `out` is exceeded.
+ */
+cg_status cg_encode(const cg_config *cfg, const uint16_t *kv, void *ws, size_t ws_bytes, const cg_encoded *out,
+                    cg_sizes *sizes, uint32_t *dev_status, void *stream);
+
+/*
+ * Decode a whole encoded object (device pointers in *enc) into kv_out
+ * (device, fp16 bits, [L][2][T][C]).  One thread block per (layer, K/V,
+ * 32-channel group) loads its 32 frequency tables into shared memory; each
+ * warp decodes one stream (one lane per channel), dequantizes and adds the
+ * anchor in fp32 and stores fp16 (the GPU decoder of the CacheGen pages,
+ * gptget.net page, method details).  Reconstruction is
+ * fp16_rn(q_a * s) for anchors and fp16_rn(q_a * s + q * step) for deltas,
+ * every fp32 operation rounded separately.
+ *   dev_status: CORRUPT when a table, offset, escape count, end state or
+ *               padding check fails.
+ */
+cg_status cg_decode(const cg_config *cfg, const cg_encoded *enc, uint16_t *kv_out, uint32_t *dev_status,
+                    void *stream);
+
+/* One chunk to decode: chunk `chunk` of object `enc` (configured by `cfg`)
+ * is written to dst, a device fp16 tensor [L][2][dst_tokens][C], at token
+ * rows dst_token0 .. dst_token0 + chunk length - 1.  The encoded object's
+ * sections may be the full object or just device copies whose per-chunk
+ * ranges for this chunk are present (see cg_chunk_ranges). */
+typedef struct {
+    const cg_config *cfg;
+    const cg_encoded *enc;
+    uint32_t chunk;
+    uint16_t *dst;
+    uint32_t dst_tokens;
+    uint32_t dst_token0;
+} cg_chunk_ref;
+
+/* Workspace bytes cg_decode_chunks needs for these refs.  Host only. */
+cg_status cg_decode_chunks_ws_bytes(const cg_chunk_ref *refs, uint32_t n, size_t *ws_bytes);
+
+/*
+ * Decode a batch of chunks, possibly from different objects (e.g. the
+ * quality level chosen per chunk, "CacheGen vs 传统量化KV缓存压缩技术深度对比
+ * 与性能测试", §2.2), in one launch.  Chunks of the same object share the
+ * thread blocks that load that object's tables.
+ *   ws: device workspace of cg_decode_chunks_ws_bytes bytes, 256-aligned;
+ *       it receives the job descriptors (copied from host memory that is
+ *       released before the call returns).
+ */
+cg_status cg_decode_chunks(const cg_chunk_ref *refs, uint32_t n, void *ws, size_t ws_bytes, uint32_t *dev_status,
+                           void *stream);
+
+/* Where chunk `chunk` lives inside the per-chunk sections: byte ranges of
+ * payload and anchors, entry range of escapes, and entry ranges of
+ * stream_off / esc_off that describe it.  Host only; `off` arrays are host
+ * copies of stream_off (u64) and esc_off (u32) of the object. */
+typedef struct {
+    uint64_t stream_begin, stream_end;   /* stream indices */
+    uint64_t payload_begin, payload_end; /* bytes */
+    uint64_t escape_begin, escape_end;   /* entries */
+    uint64_t anchor_begin, anchor_end;   /* bytes */
+} cg_chunk_range;
+cg_status cg_chunk_ranges(const cg_config *cfg, uint32_t chunk, const uint64_t *stream_off, const uint32_t *esc_off,
+                          cg_chunk_range *r);
+
+/*
+ * Serialized object: a header (magic "CGKV", version, L, T, C, group_size,
+ * chunk_tokens, tokens_per_stream, the L steps, section sizes) followed by
+ * the sections of `obj` (host pointers) in the order listed at the top of
+ * this file.  cg_serialize with buf == NULL reports the size in *len.
+ */
+cg_status cg_serialize(const cg_config *cfg, const cg_encoded *obj, const cg_sizes *sizes, void *buf, size_t *len);
+
+/* Read a serialized header: fills cfg (cfg->step is set to `step`, which
+ * must hold CG_MAX_LAYERS floats or at least L) and *sizes. */
+cg_status cg_deserialize_header(const void *buf, size_t len, cg_config *cfg, float *step, cg_sizes *sizes);
+
+/* Copy the sections of a serialized object into `obj` (host pointers with
+ * capacities at least the sizes from cg_deserialize_header). */
+cg_status cg_deserialize(const void *buf, size_t len, const cg_encoded *obj);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CG_H */

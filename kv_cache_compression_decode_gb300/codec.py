@@ -1,0 +1,374 @@
+"""Python binding of libcg (the codec's C ABI in include/cg.h).
+
+Argument marshalling only: every step of the codec runs in libcg's CUDA
+kernels.  PyTorch supplies device memory, pinned host memory and streams.
+The functions keep the C names (cg_encode, cg_decode, ...); a few helpers
+(`alloc_encoded`, `encode`, `decode`) only size and allocate buffers around
+those calls.  There is no CPU fallback: if libcg.so cannot be built or loaded,
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes as ct
+import dataclasses
+from typing import List, Optional, Sequence, Tuple
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+CG_OK, CG_ERR_INVALID_ARG, CG_ERR_NONFINITE, CG_ERR_RANGE = 0, 1, 2, 3
+CG_ERR_CORRUPT, CG_ERR_TIMEOUT, CG_ERR_CUDA = 4, 5, 6
+CG_MAX_LAYERS = 1024
+
+# Step per layer third: shallow / middle / deep ("CacheGen vs 传统量化KV缓存压缩
+# 技术深度对比与性能测试", §1 and §2.1, layer-sensitive quantization).
+LAYER_BASE_STEPS = (0.5, 1.0, 1.5)
+
+
+def layer_steps(L: int, base: Sequence[float] = LAYER_BASE_STEPS, mult: float = 1.0) -> np.ndarray:
+    """Quantization step of each layer: base[floor(3 l / L)] * mult, fp32."""
+    b = np.asarray(base, dtype=np.float32)
+    return np.array([b[(3 * l) // L] * np.float32(mult) for l in range(L)], dtype=np.float32)
+
+
+class cg_config(ct.Structure):
+    _fields_ = [("L", ct.c_uint32), ("T", ct.c_uint32), ("C", ct.c_uint32), ("group_size", ct.c_uint32),
+                ("chunk_tokens", ct.c_uint32), ("tokens_per_stream", ct.c_uint32),
+                ("step", ct.POINTER(ct.c_float))]
+
+
+class cg_bounds(ct.Structure):
+    _fields_ = [(n, ct.c_uint64) for n in (
+        "A", "n_chunks", "spans_total", "n_streams", "n_tables", "anchors_bytes", "scales_bytes",
+        "table_off_bytes", "tables_max_bytes", "stream_off_bytes", "payload_max_bytes", "esc_off_bytes",
+        "escapes_max_count", "workspace_bytes")]
+
+    def as_dict(self) -> dict:
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+class cg_encoded(ct.Structure):
+    _fields_ = [("anchors", ct.c_void_p), ("scales", ct.c_void_p), ("tables", ct.c_void_p),
+                ("table_off", ct.c_void_p), ("payload", ct.c_void_p), ("stream_off", ct.c_void_p),
+                ("escapes", ct.c_void_p), ("esc_off", ct.c_void_p), ("tables_cap", ct.c_uint64),
+                ("payload_cap", ct.c_uint64), ("escapes_cap", ct.c_uint64)]
+
+
+class cg_sizes(ct.Structure):
+    _fields_ = [("payload_bytes", ct.c_uint64), ("tables_bytes", ct.c_uint64), ("n_escapes", ct.c_uint64),
+                ("total_bytes", ct.c_uint64)]
+
+
+class cg_chunk_ref(ct.Structure):
+    _fields_ = [("cfg", ct.POINTER(cg_config)), ("enc", ct.POINTER(cg_encoded)), ("chunk", ct.c_uint32),
+                ("dst", ct.c_void_p), ("dst_tokens", ct.c_uint32), ("dst_token0", ct.c_uint32)]
+
+
+class cg_chunk_range(ct.Structure):
+    _fields_ = [(n, ct.c_uint64) for n in (
+        "stream_begin", "stream_end", "payload_begin", "payload_end", "escape_begin", "escape_end",
+        "anchor_begin", "anchor_end")]
+
+
+# Every symbol libcg exports (the declarations of include/cg.h).
+EXPORTS = ("cg_status_string", "cg_status_from_flags", "cg_encode_bounds", "cg_encode", "cg_decode",
+           "cg_decode_chunks_ws_bytes", "cg_decode_chunks", "cg_chunk_ranges", "cg_serialize",
+           "cg_deserialize_header", "cg_deserialize")
+
+_lib = None
+
+
+def lib() -> ct.CDLL:
+    """Load libcg.so (building it first if its sources are newer)."""
+    global _lib
+    if _lib is None:
+        L = ct.CDLL(_build.build())
+        P, U32, U64 = ct.c_void_p, ct.c_uint32, ct.c_uint64
+        L.cg_status_string.restype = ct.c_char_p
+        L.cg_status_string.argtypes = [ct.c_int]
+        L.cg_status_from_flags.argtypes = [U32]
+        L.cg_encode_bounds.argtypes = [ct.POINTER(cg_config), ct.POINTER(cg_bounds)]
+        L.cg_encode.argtypes = [ct.POINTER(cg_config), P, P, ct.c_size_t, ct.POINTER(cg_encoded),
+                                ct.POINTER(cg_sizes), P, P]
+        L.cg_decode.argtypes = [ct.POINTER(cg_config), ct.POINTER(cg_encoded), P, P, P]
+        L.cg_decode_chunks_ws_bytes.argtypes = [ct.POINTER(cg_chunk_ref), U32, ct.POINTER(ct.c_size_t)]
+        L.cg_decode_chunks.argtypes = [ct.POINTER(cg_chunk_ref), U32, P, ct.c_size_t, P, P]
+        L.cg_chunk_ranges.argtypes = [ct.POINTER(cg_config), U32, P, P, ct.POINTER(cg_chunk_range)]
+        L.cg_serialize.argtypes = [ct.POINTER(cg_config), ct.POINTER(cg_encoded), ct.POINTER(cg_sizes), P,
+                                   ct.POINTER(ct.c_size_t)]
+        L.cg_deserialize_header.argtypes = [P, ct.c_size_t, ct.POINTER(cg_config), P, ct.POINTER(cg_sizes)]
+        L.cg_deserialize.argtypes = [P, ct.c_size_t, ct.POINTER(cg_encoded)]
+        for name in EXPORTS:
+            if name not in ("cg_status_string",):
+                getattr(L, name).restype = ct.c_int
+        _lib = L
+    return _lib
+
+
+class CodecError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {cg_status_string(code)} ({code})")
+        self.code = code
+
+
+def cg_status_string(code: int) -> str:
+    return lib().cg_status_string(int(code)).decode()
+
+
+def cg_status_from_flags(flags: int) -> int:
+    return int(lib().cg_status_from_flags(int(flags) & 0xFFFFFFFF))
+
+
+def _check(code: int, what: str) -> None:
+    if code != CG_OK:
+        raise CodecError(code, what)
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+@dataclasses.dataclass
+class Config:
+    """Codec configuration (mirrors cg_config); `step` is the per-layer step."""
+    L: int
+    T: int
+    C: int
+    group_size: int = 10
+    chunk_tokens: int = 0          # 0: one chunk covering all T tokens
+    tokens_per_stream: int = 1536
+    step: Optional[np.ndarray] = None
+
+    def __post_init__(self):
+        if self.step is None:
+            self.step = layer_steps(self.L)
+        self.step = np.ascontiguousarray(self.step, dtype=np.float32)
+        if not self.chunk_tokens:
+            self.chunk_tokens = self.T
+        self._c = cg_config(self.L, self.T, self.C, self.group_size, self.chunk_tokens, self.tokens_per_stream,
+                            self.step.ctypes.data_as(ct.POINTER(ct.c_float)))
+
+    def c(self) -> cg_config:
+        return self._c
+
+
+def cg_encode_bounds(cfg: Config) -> dict:
+    b = cg_bounds()
+    _check(lib().cg_encode_bounds(ct.byref(cfg.c()), ct.byref(b)), "cg_encode_bounds")
+    return b.as_dict()
+
+
+@dataclasses.dataclass
+class Encoded:
+    """The sections of an encoded object as torch tensors (device or host)."""
+    anchors: torch.Tensor     # int8
+    scales: torch.Tensor      # float32
+    tables: torch.Tensor      # uint8
+    table_off: torch.Tensor   # int32 (u32 bits)
+    payload: torch.Tensor     # uint8
+    stream_off: torch.Tensor  # int64 (u64 bits)
+    escapes: torch.Tensor     # int32
+    esc_off: torch.Tensor     # int32 (u32 bits)
+    sizes: Optional[dict] = None
+
+    def c(self) -> cg_encoded:
+        def ptr(t):
+            return t.data_ptr() if t.numel() else None
+        self._c = cg_encoded(ptr(self.anchors), ptr(self.scales), ptr(self.tables), ptr(self.table_off),
+                             ptr(self.payload), ptr(self.stream_off), ptr(self.escapes), ptr(self.esc_off),
+                             self.tables.numel(), self.payload.numel(), self.escapes.numel())
+        return self._c
+
+    def fields(self):
+        return ["anchors", "scales", "tables", "table_off", "payload", "stream_off", "escapes", "esc_off"]
+
+    def to(self, device, non_blocking=False) -> "Encoded":
+        kw = dict(device=device, non_blocking=non_blocking)
+        e = Encoded(*[getattr(self, f).to(**kw) for f in self.fields()], sizes=self.sizes)
+        return e
+
+    def trimmed(self) -> "Encoded":
+        """Views cut to the actual sizes (after an encode has completed)."""
+        s = self.sizes
+        return Encoded(self.anchors, self.scales, self.tables[: s["tables_bytes"]], self.table_off,
+                       self.payload[: s["payload_bytes"]], self.stream_off, self.escapes[: s["n_escapes"]],
+                       self.esc_off, sizes=s)
+
+
+def alloc_encoded(cfg: Config, device="cuda", escapes_cap: Optional[int] = None, pin: bool = False) -> Encoded:
+    """Allocate output sections for cg_encode with worst-case capacities
+    (escapes default to one per 64 delta values plus 4096; cg_encode flags
+    CG_ERR_RANGE if that is not enough)."""
+    b = cg_encode_bounds(cfg)
+    if escapes_cap is None:
+        escapes_cap = min(b["escapes_max_count"], b["escapes_max_count"] // 64 + 4096)
+    kw = dict(device=device, pin_memory=pin) if device == "cpu" else dict(device=device)
+
+    def e(n, dt):
+        return torch.empty(int(n), dtype=dt, **kw)
+    return Encoded(e(b["anchors_bytes"], torch.int8), e(b["scales_bytes"] // 4, torch.float32),
+                   e(max(b["tables_max_bytes"], 1), torch.uint8), e(b["n_tables"] + 1, torch.int32),
+                   e(max(b["payload_max_bytes"], 16), torch.uint8), e(b["n_streams"] + 1, torch.int64),
+                   e(max(escapes_cap, 1), torch.int32), e(b["n_streams"] + 1, torch.int32))
+
+
+def cg_encode(cfg: Config, kv: torch.Tensor, ws: torch.Tensor, out: Encoded, sizes_host: ct.Structure,
+              status: torch.Tensor, stream=None) -> None:
+    """Enqueue cg_encode.  kv: device fp16 [L][2][T][C]; ws: device uint8
+    workspace; sizes_host: a cg_sizes in (ideally pinned) host memory;
+    status: device int32[1] cleared by the caller."""
+    assert kv.is_cuda and kv.dtype == torch.float16 and kv.is_contiguous()
+    assert tuple(kv.shape) == (cfg.L, 2, cfg.T, cfg.C)
+    code = lib().cg_encode(ct.byref(cfg.c()), kv.data_ptr(), ws.data_ptr(), ws.numel(), ct.byref(out.c()),
+                           ct.byref(sizes_host), status.data_ptr(), _stream_ptr(stream))
+    _check(code, "cg_encode")
+
+
+def cg_decode(cfg: Config, enc: Encoded, kv_out: torch.Tensor, status: torch.Tensor, stream=None) -> None:
+    """Enqueue cg_decode of a whole object into kv_out (device fp16 [L][2][T][C])."""
+    assert kv_out.is_cuda and kv_out.dtype == torch.float16 and kv_out.is_contiguous()
+    assert tuple(kv_out.shape) == (cfg.L, 2, cfg.T, cfg.C)
+    code = lib().cg_decode(ct.byref(cfg.c()), ct.byref(enc.c()), kv_out.data_ptr(), status.data_ptr(),
+                           _stream_ptr(stream))
+    _check(code, "cg_decode")
+
+
+@dataclasses.dataclass
+class ChunkRef:
+    cfg: Config
+    enc: Encoded
+    chunk: int
+    dst: torch.Tensor      # device fp16 [L][2][dst_tokens][C]
+    dst_token0: int
+
+
+def _refs(refs: Sequence[ChunkRef]):
+    encs = {}
+    arr = (cg_chunk_ref * len(refs))()
+    keep = []
+    for i, r in enumerate(refs):
+        key = id(r.enc)
+        if key not in encs:
+            encs[key] = r.enc.c()
+            keep.append(encs[key])
+        keep.append(r.cfg.c())
+        arr[i] = cg_chunk_ref(ct.pointer(r.cfg.c()), ct.pointer(encs[key]), r.chunk, r.dst.data_ptr(),
+                              r.dst.shape[2], r.dst_token0)
+    return arr, keep
+
+
+def cg_decode_chunks_ws_bytes(refs: Sequence[ChunkRef]) -> int:
+    arr, keep = _refs(refs)
+    n = ct.c_size_t()
+    _check(lib().cg_decode_chunks_ws_bytes(arr, len(refs), ct.byref(n)), "cg_decode_chunks_ws_bytes")
+    return int(n.value)
+
+
+def cg_decode_chunks(refs: Sequence[ChunkRef], ws: torch.Tensor, status: torch.Tensor, stream=None) -> None:
+    arr, keep = _refs(refs)
+    code = lib().cg_decode_chunks(arr, len(refs), ws.data_ptr(), ws.numel(), status.data_ptr(),
+                                  _stream_ptr(stream))
+    _check(code, "cg_decode_chunks")
+
+
+def cg_chunk_ranges(cfg: Config, chunk: int, stream_off: np.ndarray, esc_off: np.ndarray) -> dict:
+    so = np.ascontiguousarray(stream_off, dtype=np.uint64)
+    eo = np.ascontiguousarray(esc_off, dtype=np.uint32)
+    r = cg_chunk_range()
+    _check(lib().cg_chunk_ranges(ct.byref(cfg.c()), chunk, so.ctypes.data, eo.ctypes.data, ct.byref(r)),
+           "cg_chunk_ranges")
+    return {n: int(getattr(r, n)) for n, _ in r._fields_}
+
+
+def cg_serialize(cfg: Config, host: Encoded) -> bytes:
+    s = host.sizes
+    sz = cg_sizes(s["payload_bytes"], s["tables_bytes"], s["n_escapes"], s["total_bytes"])
+    n = ct.c_size_t()
+    _check(lib().cg_serialize(ct.byref(cfg.c()), None, ct.byref(sz), None, ct.byref(n)), "cg_serialize")
+    buf = ct.create_string_buffer(n.value)
+    _check(lib().cg_serialize(ct.byref(cfg.c()), ct.byref(host.c()), ct.byref(sz), buf, ct.byref(n)),
+           "cg_serialize")
+    return buf.raw[: n.value]
+
+
+def cg_deserialize(buf: bytes) -> Tuple[Config, Encoded]:
+    c = cg_config()
+    step = (ct.c_float * CG_MAX_LAYERS)()
+    sz = cg_sizes()
+    _check(lib().cg_deserialize_header(buf, len(buf), ct.byref(c), step, ct.byref(sz)), "cg_deserialize_header")
+    cfg = Config(c.L, c.T, c.C, c.group_size, c.chunk_tokens, c.tokens_per_stream,
+                 np.array(step[: c.L], dtype=np.float32))
+    b = cg_encode_bounds(cfg)
+    e = lambda n, dt: torch.empty(int(n), dtype=dt)
+    host = Encoded(e(b["anchors_bytes"], torch.int8), e(b["scales_bytes"] // 4, torch.float32),
+                   e(sz.tables_bytes, torch.uint8), e(b["n_tables"] + 1, torch.int32),
+                   e(sz.payload_bytes, torch.uint8), e(b["n_streams"] + 1, torch.int64),
+                   e(sz.n_escapes, torch.int32), e(b["n_streams"] + 1, torch.int32),
+                   sizes={"payload_bytes": sz.payload_bytes, "tables_bytes": sz.tables_bytes,
+                          "n_escapes": sz.n_escapes, "total_bytes": sz.total_bytes})
+    _check(lib().cg_deserialize(buf, len(buf), ct.byref(host.c())), "cg_deserialize")
+    return cfg, host
+
+
+# ---------------------------------------------------------------------------
+# Allocation helpers around the calls above (sizing and plumbing only)
+# ---------------------------------------------------------------------------
+
+def new_status(device="cuda") -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def read_status(status: torch.Tensor) -> int:
+    return cg_status_from_flags(int(status.item()))
+
+
+class Encoder:
+    """Holds the workspace, output buffers and pinned sizes for one config."""
+
+    def __init__(self, cfg: Config, device="cuda", escapes_cap: Optional[int] = None):
+        self.cfg = cfg
+        self.bounds = cg_encode_bounds(cfg)
+        self.ws = torch.empty(self.bounds["workspace_bytes"], dtype=torch.uint8, device=device)
+        self.out = alloc_encoded(cfg, device, escapes_cap)
+        self.sizes_buf = torch.zeros(4, dtype=torch.int64, pin_memory=True)
+        self.sizes = cg_sizes.from_address(self.sizes_buf.data_ptr())
+        self.status = new_status(device)
+
+    def launch(self, kv: torch.Tensor, stream=None) -> None:
+        cg_encode(self.cfg, kv, self.ws, self.out, self.sizes, self.status, stream)
+
+    def result(self) -> Encoded:
+        """After the stream has completed: the sizes and trimmed sections."""
+        self.out.sizes = {"payload_bytes": int(self.sizes.payload_bytes), "tables_bytes": int(self.sizes.tables_bytes),
+                          "n_escapes": int(self.sizes.n_escapes), "total_bytes": int(self.sizes.total_bytes)}
+        return self.out.trimmed()
+
+
+def encode(cfg: Config, kv: torch.Tensor, stream=None) -> Encoded:
+    """Encode a device cache and wait for it; raises on any device status."""
+    enc = Encoder(cfg, kv.device)
+    enc.launch(kv, stream)
+    torch.cuda.synchronize(kv.device)
+    st = read_status(enc.status)
+    if st == CG_ERR_RANGE and enc.sizes.n_escapes > enc.out.escapes.numel():
+        enc = Encoder(cfg, kv.device, escapes_cap=int(enc.sizes.n_escapes))
+        enc.launch(kv, stream)
+        torch.cuda.synchronize(kv.device)
+        st = read_status(enc.status)
+    _check(st, "cg_encode (device)")
+    return enc.result()
+
+
+def decode(cfg: Config, enc: Encoded, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode a device object and wait for it; raises on any device status."""
+    dev = enc.payload.device
+    if out is None:
+        out = torch.empty((cfg.L, 2, cfg.T, cfg.C), dtype=torch.float16, device=dev)
+    status = new_status(dev)
+    cg_decode(cfg, enc, out, status, stream)
+    torch.cuda.synchronize(dev)
+    _check(read_status(status), "cg_decode (device)")
+    return out

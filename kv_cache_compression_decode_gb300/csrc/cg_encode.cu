@@ -1,0 +1,482 @@
+// cg_encode.cu -- GPU encoder of the KV-cache codec (sm_103a).
+//
+// Pipeline (the CacheGen compression pipeline: anchor/delta, layer-binned
+// quantization, arithmetic coding with per-(layer, channel) statistics;
+// "CacheGen vs 传统量化KV缓存压缩技术深度对比与性能测试", §1 and §2.1):
+//   k_stats   one block per (32-channel group, layer, K/V): anchor absmax ->
+//             scale, int8 anchors, delta quantization, shared-memory
+//             histograms (lane = channel, bank = lane: conflict-free
+//             atomics), escape counts per stream, normalization of the 32
+//             histograms to 16-bit frequency tables (warp-cooperative).
+//   k_scan    exclusive scans of table sizes, escape counts and stream sizes.
+//   k_encode  one warp per stream (lane = channel): interleaved range ANS
+//             over the span's delta tokens in reverse, words written
+//             backwards into a per-stream scratch region, escapes placed
+//             from the end of the stream's escape range.
+//   k_pack    one warp per stream: copies the stream words into the
+//             payload at its prefix-sum offset, zero-padded to 16 bytes.
+#include <cuda_fp16.h>
+
+#include "cg_internal.cuh"
+
+namespace cg {
+
+struct StepTable {
+    float v[CG_MAX_LAYERS];
+};
+
+struct EncArgs {
+    Geom g;
+    const uint16_t *kv;
+    int8_t *anchors;
+    float *scales;
+    uint8_t *tables;
+    uint32_t *table_off;
+    uint8_t *payload;
+    uint64_t *stream_off;
+    int32_t *escapes;
+    uint32_t *esc_off;
+    uint64_t tables_cap, payload_cap, escapes_cap;
+    // workspace
+    uint16_t *ftab;        // [n_tables][256] f - 1
+    uint32_t *tlohi;       // [n_tables] lo | hi << 8
+    uint32_t *twidth;      // [n_tables] compact table bytes
+    uint32_t *esc_count;   // [n_streams]
+    uint32_t *words_count; // [n_streams]
+    uint16_t *scratch;     // [n_streams][region_words]
+    uint64_t region_words;
+    cg_sizes *dsizes;
+    uint32_t *status;
+};
+
+// Workspace carving (256-byte aligned pieces).
+struct WsLayout {
+    uint64_t ftab, tlohi, twidth, esc_count, words_count, scratch, dsizes, total, region_words;
+};
+
+static WsLayout ws_layout(const Geom &g) {
+    WsLayout w;
+    uint64_t o = 0;
+    auto take = [&](uint64_t bytes) {
+        uint64_t at = o;
+        o = round_up(o + bytes, 256);
+        return at;
+    };
+    w.region_words = round_up((uint64_t)kLanes * (g.tps + 2u), 8);
+    w.ftab = take(g.n_tables * 256u * 2u);
+    w.tlohi = take(g.n_tables * 4u);
+    w.twidth = take(g.n_tables * 4u);
+    w.esc_count = take(g.n_streams * 4u);
+    w.words_count = take(g.n_streams * 4u);
+    w.scratch = take(g.n_streams * w.region_words * 2u);
+    w.dsizes = take(sizeof(cg_sizes));
+    w.total = o;
+    return w;
+}
+
+__device__ __forceinline__ float ld_half(const uint16_t *p) { return __half2float(__ushort_as_half(*p)); }
+
+__device__ __forceinline__ uint32_t symbol_of(int q) {
+    return (uint32_t)(q + 127) <= 254u ? (uint32_t)(q + 127) : kEsc;
+}
+
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// (value, symbol) argmax, smallest symbol on a tie.
+__device__ __forceinline__ void warp_argmax(uint32_t &v, uint32_t &s) {
+    for (int o = 16; o; o >>= 1) {
+        uint32_t ov = __shfl_xor_sync(kFull, v, o), os = __shfl_xor_sync(kFull, s, o);
+        if (ov > v || (ov == v && os < s)) {
+            v = ov;
+            s = os;
+        }
+    }
+}
+
+constexpr int kStatsWarps = 8;
+
+__global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable st) {
+    const Geom &g = a.g;
+    const uint32_t grp = blockIdx.x, slice = blockIdx.y;
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    const uint32_t c = grp * kLanes + lane;
+    const uint16_t *x = a.kv + (uint64_t)slice * g.T * g.C + c;
+    const float step = st.v[slice >> 1];
+
+    __shared__ uint32_t hist[256 * kLanes];  // [symbol][lane]
+    __shared__ float red[kStatsWarps][kLanes];
+    __shared__ float s_scale[kLanes];
+
+    for (uint32_t i = threadIdx.x; i < 256u * kLanes; i += blockDim.x) hist[i] = 0;
+
+    // E1: absmax over this call's anchor rows -> scale = absmax / 127.
+    float amax = 0.f;
+    for (uint64_t r = warp; r < g.A; r += kStatsWarps) {
+        uint32_t ch = (uint32_t)(r / g.apc_full), ar = (uint32_t)(r - (uint64_t)ch * g.apc_full);
+        uint32_t t = ch * g.chunk + ar * g.G;
+        amax = fmaxf(amax, fabsf(ld_half(x + (uint64_t)t * g.C)));
+    }
+    red[warp][lane] = amax;
+    __syncthreads();
+    if (warp == 0) {
+        float m = red[0][lane];
+        for (int w = 1; w < kStatsWarps; w++) m = fmaxf(m, red[w][lane]);
+        float s = m > 0.f ? __fdiv_rn(m, 127.f) : 1.f;
+        s_scale[lane] = s;
+        a.scales[(uint64_t)slice * g.C + c] = s;
+    }
+    __syncthreads();
+    const float sa = s_scale[lane];
+
+    // E2 + E3 + E4: one warp per group of tokens (anchor + its deltas).
+    bool nonfinite = false;
+    for (uint64_t r = warp; r < g.A; r += kStatsWarps) {
+        uint32_t ch = (uint32_t)(r / g.apc_full), ar = (uint32_t)(r - (uint64_t)ch * g.apc_full);
+        uint32_t c0 = ch * g.chunk, len = g.chunk_len(ch);
+        uint32_t p0 = ar * g.G, p1 = min(p0 + g.G, len);
+        float v = ld_half(x + (uint64_t)(c0 + p0) * g.C);
+        nonfinite |= !isfinite(v);
+        float qa = fminf(fmaxf(rintf(__fdiv_rn(v, sa)), -127.f), 127.f);
+        a.anchors[g.anchor_index(slice, c0 + p0) + c] = (int8_t)qa;
+        float xa = __fmul_rn(qa, sa);
+        for (uint32_t p = p0 + 1; p < p1; p++) {
+            v = ld_half(x + (uint64_t)(c0 + p) * g.C);
+            nonfinite |= !isfinite(v);
+            int q = __float2int_rn(__fdiv_rn(__fsub_rn(v, xa), step));
+            uint32_t s = symbol_of(q);
+            atomicAdd(&hist[s * kLanes + lane], 1u);
+            if (s == kEsc) atomicAdd(&a.esc_count[g.stream_index(ch, slice, p / g.tps, grp)], 1u);
+        }
+    }
+    if (__any_sync(kFull, nonfinite) && lane == 0) flag(a.status, CG_ERR_NONFINITE);
+    __syncthreads();
+
+    // E5: normalize each channel's counts to a 16-bit table (warp per channel).
+    for (uint32_t j = warp; j < kLanes; j += kStatsWarps) {
+        const uint64_t table = (uint64_t)slice * g.C + grp * kLanes + j;
+        uint32_t n[8], f[8];
+        uint32_t N = 0, lo = 256, hi = 0;
+        bool any = false;
+        for (int i = 0; i < 8; i++) {
+            uint32_t s = (uint32_t)i * 32u + lane;
+            n[i] = hist[s * kLanes + j];
+            N += n[i];
+            if (n[i]) {
+                lo = min(lo, s);
+                hi = max(hi, s);
+                any = true;
+            }
+        }
+        N = warp_sum(N);
+        for (int o = 16; o; o >>= 1) {
+            lo = min(lo, __shfl_xor_sync(kFull, lo, o));
+            hi = max(hi, __shfl_xor_sync(kFull, hi, o));
+        }
+        any = __any_sync(kFull, any);
+        if (!any) {
+            if (lane == 0) {
+                a.tlohi[table] = 1u;
+                a.twidth[table] = 2u;
+            }
+            continue;
+        }
+        uint32_t sum = 0, bn = 0, bs = 256;
+        for (int i = 0; i < 8; i++) {
+            uint32_t s = (uint32_t)i * 32u + lane;
+            f[i] = 0;
+            if (s >= lo && s <= hi) {
+                uint64_t v = ((uint64_t)n[i] * kM) / N;
+                f[i] = v < 1u ? 1u : (uint32_t)v;
+            }
+            sum += f[i];
+            if (n[i] > bn) {
+                bn = n[i];
+                bs = s;
+            }
+        }
+        sum = warp_sum(sum);
+        int R = (int)kM - (int)sum;
+        if (R > 0) {
+            warp_argmax(bn, bs);
+            if ((bs & 31u) == lane) f[bs >> 5] += (uint32_t)R;
+        }
+        for (int guard = 0; R < 0 && guard < 512; guard++) {
+            uint32_t bf = 0, bfs = 256;
+            for (int i = 0; i < 8; i++)
+                if (f[i] > bf) {
+                    bf = f[i];
+                    bfs = (uint32_t)i * 32u + lane;
+                }
+            warp_argmax(bf, bfs);
+            int dec = min((int)bf - 1, -R);
+            if (dec <= 0) break;
+            if ((bfs & 31u) == lane) f[bfs >> 5] -= (uint32_t)dec;
+            R += dec;
+        }
+        for (int i = 0; i < 8; i++) {
+            uint32_t s = (uint32_t)i * 32u + lane;
+            if (s >= lo && s <= hi) a.ftab[table * 256u + s] = (uint16_t)(f[i] - 1u);
+        }
+        if (lane == 0) {
+            a.tlohi[table] = lo | (hi << 8);
+            a.twidth[table] = 2u + 2u * (hi - lo + 1u);
+        }
+    }
+}
+
+// Exclusive scan of n u32 values (optionally padded-words -> bytes) into
+// out[0..n] with a single block; flags RANGE if the total exceeds `cap` or
+// the output type.
+template <typename OutT, bool kWordsToBytes>
+__global__ void __launch_bounds__(1024) k_scan(const uint32_t *in, uint64_t n, OutT *out, uint64_t cap,
+                                               uint32_t *status) {
+    __shared__ uint64_t part[1024];
+    const uint32_t tid = threadIdx.x;
+    const uint64_t per = (n + 1023u) / 1024u;
+    const uint64_t b = min((uint64_t)tid * per, n), e = min(b + per, n);
+    auto xf = [](uint32_t v) -> uint64_t { return kWordsToBytes ? round_up(v, 8) * 2u : (uint64_t)v; };
+    uint64_t s = 0;
+    for (uint64_t i = b; i < e; i++) s += xf(in[i]);
+    part[tid] = s;
+    __syncthreads();
+    for (uint32_t o = 1; o < 1024; o <<= 1) {
+        uint64_t v = tid >= o ? part[tid - o] : 0;
+        __syncthreads();
+        part[tid] += v;
+        __syncthreads();
+    }
+    uint64_t run = part[tid] - s;
+    for (uint64_t i = b; i < e; i++) {
+        out[i] = (OutT)run;
+        run += xf(in[i]);
+    }
+    if (tid == 1023) {
+        uint64_t total = part[1023];
+        out[n] = (OutT)total;
+        if (total > cap || total > (uint64_t)(OutT)~(OutT)0) flag(status, CG_ERR_RANGE);
+    }
+}
+
+constexpr int kEncWarps = 8;
+
+__global__ void __launch_bounds__(kEncWarps * 32) k_encode(EncArgs a, StepTable st) {
+    const Geom &g = a.g;
+    const uint32_t grp = blockIdx.x, slice = blockIdx.y;
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    const uint32_t c = grp * kLanes + lane;
+    const uint16_t *x = a.kv + (uint64_t)slice * g.T * g.C + c;
+    const float step = st.v[slice >> 1];
+    const uint32_t lt = lanemask_lt();
+
+    __shared__ uint32_t etab[256 * kLanes];  // [symbol][lane]: c | (f - 1) << 16
+    __shared__ float s_scale[kLanes];
+
+    if (warp == 0) {
+        const uint64_t table = (uint64_t)slice * g.C + c;
+        const uint32_t lh = a.tlohi[table], lo = lh & 255u, hi = (lh >> 8) & 255u;
+        const uint64_t off = a.table_off[table];
+        const bool fits = off + a.twidth[table] <= a.tables_cap;
+        if (fits) {
+            a.tables[off] = (uint8_t)lo;
+            a.tables[off + 1] = (uint8_t)hi;
+        }
+        uint32_t cum = 0;
+        for (uint32_t s = lo; s <= hi; s++) {
+            uint32_t fm1 = a.ftab[table * 256u + s];
+            etab[s * kLanes + lane] = cum | (fm1 << 16);
+            if (fits) {
+                a.tables[off + 2u + 2u * (s - lo)] = (uint8_t)(fm1 & 255u);
+                a.tables[off + 3u + 2u * (s - lo)] = (uint8_t)(fm1 >> 8);
+            }
+            cum += fm1 + 1u;
+        }
+        s_scale[lane] = a.scales[(uint64_t)slice * g.C + c];
+    }
+    __syncthreads();
+    const float sa = s_scale[lane];
+
+    for (uint64_t sp = warp; sp < g.spans_total; sp += kEncWarps) {
+        const uint32_t ch = (uint32_t)(sp / g.spans_full), span = (uint32_t)(sp - (uint64_t)ch * g.spans_full);
+        const uint32_t c0 = ch * g.chunk, len = g.chunk_len(ch);
+        const uint32_t p0 = span * g.tps, p1 = min(p0 + g.tps, len);
+        const uint64_t k = g.stream_index(ch, slice, span, grp);
+        if (g.steps_in(p0, p1) == 0) {
+            if (lane == 0) a.words_count[k] = 0;
+            continue;
+        }
+        uint16_t *region = a.scratch + k * a.region_words;
+        uint32_t top = (uint32_t)a.region_words;
+        uint32_t e_top = a.esc_count[k];
+        const uint64_t e_base = a.esc_off[k];
+        bool esc_bad = false;
+        uint32_t xs = kStateLow;
+        uint32_t gp = (p1 - 1u) % g.G;  // position in group of token p1-1
+        uint32_t row_pos = p1;          // chunk position of the anchor whose value is in xa
+        float xa = 0.f;
+        for (uint32_t p = p1; p-- > p0;) {
+            const uint32_t cur_gp = gp;
+            gp = gp == 0 ? g.G - 1u : gp - 1u;
+            if (cur_gp == 0) continue;  // anchor token: not in the stream
+            const uint32_t apos = p - cur_gp;
+            if (apos != row_pos) {
+                row_pos = apos;
+                xa = __fmul_rn((float)a.anchors[g.anchor_index(slice, c0 + apos) + c], sa);
+            }
+            const float v = ld_half(x + (uint64_t)(c0 + p) * g.C);
+            const int q = __float2int_rn(__fdiv_rn(__fsub_rn(v, xa), step));
+            const uint32_t s = symbol_of(q);
+            const uint32_t eb = __ballot_sync(kFull, s == kEsc);
+            if (eb) {
+                const uint32_t ne = __popc(eb);
+                if (ne > e_top) {
+                    esc_bad = true;
+                } else {
+                    if (s == kEsc) {
+                        uint64_t idx = e_base + e_top - ne + __popc(eb & lt);
+                        if (idx < a.escapes_cap) a.escapes[idx] = q;
+                    }
+                    e_top -= ne;
+                }
+            }
+            const uint32_t e = etab[s * kLanes + lane];
+            const uint32_t f = (e >> 16) + 1u, cs = e & 0xFFFFu;
+            const bool emit = (xs >> 16) >= f;
+            const uint32_t mb = __ballot_sync(kFull, emit);
+            const uint32_t nem = __popc(mb);
+            if (emit) {
+                region[top - nem + __popc(mb & lt)] = (uint16_t)(xs & 0xFFFFu);
+                xs >>= 16;
+            }
+            top -= nem;
+            xs = ((xs / f) << 16) + (xs % f) + cs;
+        }
+        top -= 2u * kLanes;
+        region[top + 2u * lane] = (uint16_t)(xs >> 16);
+        region[top + 2u * lane + 1u] = (uint16_t)(xs & 0xFFFFu);
+        if (lane == 0) {
+            a.words_count[k] = (uint32_t)a.region_words - top;
+            if (esc_bad || e_top != 0) flag(a.status, CG_ERR_CORRUPT);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) k_pack(EncArgs a) {
+    const uint64_t k = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t lane = threadIdx.x & 31u;
+    if (k >= a.g.n_streams) return;
+    const uint32_t cnt = a.words_count[k];
+    const uint64_t off = a.stream_off[k], end = a.stream_off[k + 1];
+    if (end > a.payload_cap) return;  // RANGE already flagged by the scan
+    const uint16_t *src = a.scratch + k * a.region_words + (a.region_words - cnt);
+    uint16_t *dst = reinterpret_cast<uint16_t *>(a.payload + off);
+    const uint64_t n = (end - off) >> 1;
+    for (uint64_t i = lane; i < n; i += 32) dst[i] = i < cnt ? src[i] : (uint16_t)0;
+}
+
+__global__ void k_sizes(EncArgs a, uint64_t fixed_bytes) {
+    cg_sizes s;
+    s.payload_bytes = a.stream_off[a.g.n_streams];
+    s.tables_bytes = a.table_off[a.g.n_tables];
+    s.n_escapes = a.esc_off[a.g.n_streams];
+    s.total_bytes = s.payload_bytes + s.tables_bytes + 4u * s.n_escapes + fixed_bytes;
+    *a.dsizes = s;
+}
+
+}  // namespace cg
+
+using namespace cg;
+
+extern "C" cg_status cg_encode_bounds(const cg_config *cfg, cg_bounds *b) {
+    Geom g;
+    if (!b || !make_geom(cfg, &g)) return CG_ERR_INVALID_ARG;
+    b->A = g.A;
+    b->n_chunks = g.n_chunks;
+    b->spans_total = g.spans_total;
+    b->n_streams = g.n_streams;
+    b->n_tables = g.n_tables;
+    b->anchors_bytes = (uint64_t)g.n_slices * g.A * g.C;
+    b->scales_bytes = g.n_tables * 4u;
+    b->table_off_bytes = (g.n_tables + 1u) * 4u;
+    b->tables_max_bytes = g.n_tables * (2u + 2u * 256u);
+    b->stream_off_bytes = (g.n_streams + 1u) * 8u;
+    b->esc_off_bytes = (g.n_streams + 1u) * 4u;
+    uint64_t words = 0;  // worst-case padded words of one slice-group column
+    for (uint32_t ch = 0; ch < g.n_chunks; ch++) {
+        uint32_t len = g.chunk_len(ch);
+        for (uint32_t p0 = 0; p0 < len; p0 += g.tps) {
+            uint32_t p1 = p0 + g.tps < len ? p0 + g.tps : len;
+            uint32_t n = g.steps_in(p0, p1);
+            if (n) words += round_up((uint64_t)kLanes * (n + 2u), 8);
+        }
+    }
+    b->payload_max_bytes = words * 2u * g.n_slices * g.NG;
+    b->escapes_max_count = (uint64_t)g.n_slices * (g.T - g.A) * g.C;
+    b->workspace_bytes = ws_layout(g).total;
+    if (b->tables_max_bytes > 0xFFFFFFFFull) return CG_ERR_RANGE;
+    return CG_OK;
+}
+
+extern "C" cg_status cg_encode(const cg_config *cfg, const uint16_t *kv, void *ws, size_t ws_bytes,
+                               const cg_encoded *out, cg_sizes *sizes, uint32_t *dev_status, void *stream) {
+    Geom g;
+    if (!make_geom(cfg, &g)) return CG_ERR_INVALID_ARG;
+    if (!kv || !ws || !out || !sizes || !out->anchors || !out->scales || !out->tables || !out->table_off ||
+        !out->stream_off || !out->esc_off || (!out->payload && out->payload_cap) ||
+        (!out->escapes && out->escapes_cap))
+        return CG_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ws) % 256u || reinterpret_cast<uintptr_t>(out->payload) % 16u)
+        return CG_ERR_INVALID_ARG;
+    cg_bounds bd;
+    cg_status bs = cg_encode_bounds(cfg, &bd);
+    if (bs != CG_OK) return bs;
+    if (ws_bytes < bd.workspace_bytes) return CG_ERR_RANGE;
+    const WsLayout L = ws_layout(g);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    EncArgs a;
+    a.g = g;
+    a.kv = kv;
+    a.anchors = out->anchors;
+    a.scales = out->scales;
+    a.tables = out->tables;
+    a.table_off = out->table_off;
+    a.payload = out->payload;
+    a.stream_off = out->stream_off;
+    a.escapes = out->escapes;
+    a.esc_off = out->esc_off;
+    a.tables_cap = out->tables_cap;
+    a.payload_cap = out->payload_cap;
+    a.escapes_cap = out->escapes_cap;
+    a.ftab = reinterpret_cast<uint16_t *>(w + L.ftab);
+    a.tlohi = reinterpret_cast<uint32_t *>(w + L.tlohi);
+    a.twidth = reinterpret_cast<uint32_t *>(w + L.twidth);
+    a.esc_count = reinterpret_cast<uint32_t *>(w + L.esc_count);
+    a.words_count = reinterpret_cast<uint32_t *>(w + L.words_count);
+    a.scratch = reinterpret_cast<uint16_t *>(w + L.scratch);
+    a.region_words = L.region_words;
+    a.dsizes = reinterpret_cast<cg_sizes *>(w + L.dsizes);
+    a.status = dev_status;
+
+    StepTable st;
+    for (uint32_t l = 0; l < g.L; l++) st.v[l] = cfg->step[l];
+
+    const dim3 grid(g.NG, g.n_slices);
+    CG_CUDA_TRY(cudaMemsetAsync(a.esc_count, 0, g.n_streams * 4u, s));
+    k_stats<<<grid, kStatsWarps * 32, 0, s>>>(a, st);
+    k_scan<uint32_t, false><<<1, 1024, 0, s>>>(a.twidth, g.n_tables, a.table_off, a.tables_cap, a.status);
+    k_scan<uint32_t, false><<<1, 1024, 0, s>>>(a.esc_count, g.n_streams, a.esc_off, a.escapes_cap, a.status);
+    k_encode<<<grid, kEncWarps * 32, 0, s>>>(a, st);
+    k_scan<uint64_t, true><<<1, 1024, 0, s>>>(a.words_count, g.n_streams, a.stream_off, a.payload_cap, a.status);
+    const uint64_t pack_blocks = (g.n_streams * 32u + 255u) / 256u;
+    k_pack<<<(unsigned)pack_blocks, 256, 0, s>>>(a);
+    const uint64_t fixed = bd.anchors_bytes + bd.scales_bytes + bd.table_off_bytes + bd.stream_off_bytes +
+                           bd.esc_off_bytes;
+    k_sizes<<<1, 1, 0, s>>>(a, fixed);
+    CG_CUDA_TRY(cudaGetLastError());
+    CG_CUDA_TRY(cudaMemcpyAsync(sizes, a.dsizes, sizeof(cg_sizes), cudaMemcpyDeviceToHost, s));
+    return CG_OK;
+}

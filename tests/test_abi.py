@@ -1,0 +1,172 @@
+"""Host-side checks of the C ABI (no GPU, no kernel launch)."""
+import ctypes as ct
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from kv_cache_compression_decode_gb300 import codec as C
+from tests import parity as P
+
+HDR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "cg.h")
+
+
+def declared_functions():
+    text = open(HDR).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cg_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert len(names) >= 11
+    lib = C.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(C.EXPORTS)
+
+
+CASES = [(4, 256, 1024, 10, 0, 1536), (2, 300, 64, 10, 128, 64), (1, 1, 32, 10, 1, 1), (2, 57, 96, 1, 57, 20),
+         (3, 1000, 128, 7, 333, 100), (80, 16384, 1024, 10, 0, 1536), (32, 16384, 1024, 10, 1536, 1536),
+         (2, 4100, 64, 10, 0, 1536)]
+
+
+@pytest.mark.parametrize("L,T,Cc,G,chunk,tps", CASES)
+def test_bounds_match_oracle_geometry(L, T, Cc, G, chunk, tps):
+    pc, oc = P.configs(L, T, Cc, G, chunk, tps)
+    b = C.cg_encode_bounds(pc)
+    g = O.geometry(oc)
+    assert b["A"] == g["A"]
+    assert b["spans_total"] == g["spans_total"]
+    assert b["n_streams"] == g["n_streams"]
+    assert b["n_tables"] == g["n_tables"]
+    assert b["tables_max_bytes"] == g["tables_max_bytes"]
+    assert b["payload_max_bytes"] == g["payload_max_bytes"]
+    assert b["escapes_max_count"] == g["escapes_max_count"]
+    assert b["anchors_bytes"] == 2 * L * g["A"] * Cc
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 4, 5, 32, 48, 80, 1024])
+@pytest.mark.parametrize("mult", [1.0, 2.0, 4.0])
+def test_layer_steps_product_matches_oracle(L, mult):
+    assert np.array_equal(C.layer_steps(L, mult=mult), O.layer_steps(L, mult=mult))
+
+
+def _cfg(**kw):
+    d = dict(L=2, T=100, C=64, group_size=10, chunk_tokens=100, tokens_per_stream=50)
+    d.update(kw)
+    step = np.array(kw.pop("step", [0.5] * d["L"]), dtype=np.float32)
+    d.pop("step", None)
+    return C.Config(d["L"], d["T"], d["C"], d["group_size"], d["chunk_tokens"], d["tokens_per_stream"], step)
+
+
+@pytest.mark.parametrize("kw", [dict(C=48), dict(C=0), dict(T=0), dict(group_size=0), dict(tokens_per_stream=0),
+                                dict(step=[0.5, 2.0 ** -10]), dict(step=[0.5, float("nan")]),
+                                dict(step=[0.5, float("inf")]), dict(step=[0.5, -1.0])])
+def test_invalid_config_rejected_on_host(kw):
+    cfg = _cfg(**kw)
+    b = C.cg_bounds()
+    assert C.lib().cg_encode_bounds(ct.byref(cfg.c()), ct.byref(b)) == C.CG_ERR_INVALID_ARG
+    enc = C.cg_encoded()
+    sz = C.cg_sizes()
+    # rejected before any CUDA call: no GPU is needed to get the status back
+    assert C.lib().cg_encode(ct.byref(cfg.c()), 1, 256, 1 << 20, ct.byref(enc), ct.byref(sz), 0, None) \
+        == C.CG_ERR_INVALID_ARG
+    assert C.lib().cg_decode(ct.byref(cfg.c()), ct.byref(enc), 1, 0, None) == C.CG_ERR_INVALID_ARG
+
+
+def test_too_many_layers_rejected():
+    cfg = _cfg(L=1025, step=[0.5] * 1025)
+    b = C.cg_bounds()
+    assert C.lib().cg_encode_bounds(ct.byref(cfg.c()), ct.byref(b)) == C.CG_ERR_INVALID_ARG
+
+
+def test_null_buffers_rejected():
+    cfg = _cfg()
+    enc = C.cg_encoded()
+    sz = C.cg_sizes()
+    assert C.lib().cg_encode(ct.byref(cfg.c()), None, 256, 1 << 20, ct.byref(enc), ct.byref(sz), 0, None) \
+        == C.CG_ERR_INVALID_ARG
+    assert C.lib().cg_decode(ct.byref(cfg.c()), ct.byref(enc), 0, 0, None) == C.CG_ERR_INVALID_ARG
+    n = ct.c_size_t()
+    assert C.lib().cg_decode_chunks_ws_bytes(None, 0, ct.byref(n)) == C.CG_ERR_INVALID_ARG
+
+
+def test_status_strings_and_flags():
+    for code in range(7):
+        assert C.cg_status_string(code)
+    assert C.cg_status_string(99) == "unknown status"
+    assert C.cg_status_from_flags(0) == C.CG_OK
+    assert C.cg_status_from_flags(1 << C.CG_ERR_CORRUPT) == C.CG_ERR_CORRUPT
+    assert C.cg_status_from_flags((1 << C.CG_ERR_CORRUPT) | (1 << C.CG_ERR_NONFINITE)) == C.CG_ERR_NONFINITE
+
+
+def _host_encoded(d, oenc):
+    def t(a):
+        view = {np.uint32: np.int32, np.uint64: np.int64}.get(a.dtype.type, a.dtype.type)
+        return torch.from_numpy(np.ascontiguousarray(a).view(view).copy())
+    return C.Encoded(*[t(d[f]) for f in P.FIELDS],
+                     sizes={"payload_bytes": d["payload"].size, "tables_bytes": d["tables"].size,
+                            "n_escapes": d["escapes"].size, "total_bytes": oenc.total_bytes})
+
+
+def test_serialize_round_trip_of_an_oracle_object():
+    from kv_cache_compression_decode_gb300 import synth
+    L, T, Cc = 2, 333, 64
+    pc, oc = P.configs(L, T, Cc, 10, 100, 64)
+    x = synth.ar1_kv(L, T, Cc, 0.95, 1, seed=3).numpy()
+    x[0, 0, 7, 3] = 300.0  # an escape
+    oenc = O.encode(oc, x)
+    d = P.oracle_to_np(oenc)
+    host = _host_encoded(d, oenc)
+    buf = C.cg_serialize(pc, host)
+    assert buf[:4] == b"CGKV"
+    cfg2, back = C.cg_deserialize(buf)
+    assert (cfg2.L, cfg2.T, cfg2.C, cfg2.group_size, cfg2.chunk_tokens, cfg2.tokens_per_stream) == \
+        (L, T, Cc, 10, 100, 64)
+    assert np.array_equal(cfg2.step, pc.step)
+    P.assert_same_object(P.gpu_to_np(back), d, "deserialized")
+    bad = bytearray(buf)
+    bad[0] = ord("X")
+    with pytest.raises(C.CodecError) as e:
+        C.cg_deserialize(bytes(bad))
+    assert e.value.code == C.CG_ERR_CORRUPT
+    with pytest.raises(C.CodecError):
+        C.cg_deserialize(buf[: len(buf) // 2])
+
+
+def test_chunk_ranges_partition_the_sections():
+    from kv_cache_compression_decode_gb300 import synth
+    L, T, Cc, chunk, tps = 3, 1000, 64, 300, 128
+    pc, oc = P.configs(L, T, Cc, 10, chunk, tps)
+    x = synth.ar1_kv(L, T, Cc, 0.9, 1, seed=5).numpy()
+    oenc = O.encode(oc, x)
+    geo = P.Geo(L, T, Cc, 10, chunk, tps)
+    prev = None
+    for ch in range(geo.n_chunks):
+        r = C.cg_chunk_ranges(pc, ch, oenc.stream_off, oenc.esc_off)
+        assert r["stream_begin"] == geo.stream0(ch)
+        assert r["anchor_begin"] == geo.row0(ch) * Cc
+        assert r["anchor_end"] - r["anchor_begin"] == 2 * L * geo.apc[ch] * Cc
+        if prev:
+            for k in ("stream", "payload", "escape", "anchor"):
+                assert r[k + "_begin"] == prev[k + "_end"]
+        prev = r
+    assert prev["payload_end"] == oenc.payload.size
+    assert prev["anchor_end"] == oenc.anchors.size
+    assert prev["stream_end"] == oenc.stream_off.size - 1
+
+
+def test_decode_chunks_plan_sizes_on_host():
+    pc, _ = P.configs(2, 1000, 64, 10, 300, 128)
+    enc = C.alloc_encoded(pc, device="cpu")
+    dst = torch.empty((2, 2, 1000, 64), dtype=torch.float16)
+    refs = [C.ChunkRef(pc, enc, ch, dst, ch * 300) for ch in range(4)]
+    assert C.cg_decode_chunks_ws_bytes(refs) > 0
+    with pytest.raises(C.CodecError):  # chunk out of range
+        C.cg_decode_chunks_ws_bytes([C.ChunkRef(pc, enc, 4, dst, 0)])
+    with pytest.raises(C.CodecError):  # destination too short for the chunk
+        C.cg_decode_chunks_ws_bytes([C.ChunkRef(pc, enc, 0, dst, 800)])

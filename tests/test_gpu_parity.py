@@ -1,0 +1,263 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bar: every section of the encoded object byte-equal, the decoded fp16 cache
+bit-equal (0 ulp).  Small cases cover several stream tiles, ragged chunks,
+spans and groups, and the degenerate cases; the full-size workloads compare
+whole layer ranges (the oracle encodes/decodes those layers on its own),
+in the same launch configuration the benchmark uses.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from kv_cache_compression_decode_gb300 import codec as C
+from kv_cache_compression_decode_gb300 import synth
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+needs_gpu = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
+
+
+def _roundtrip_check(L, T, Cc, G, chunk, tps, x_cpu, mult=1.0, step=None):
+    pc, oc = P.configs(L, T, Cc, G, chunk, tps, mult)
+    if step is not None:
+        pc = C.Config(L, T, Cc, G, chunk or T, tps, np.asarray(step, np.float32))
+        oc = O.Config(L, T, Cc, G, chunk or T, tps, np.asarray(step, np.float32))
+    x16 = x_cpu.numpy().view(np.uint16)
+    oenc = O.encode(oc, x16, nthreads=P.nthreads())
+    odec = O.decode(oc, oenc, nthreads=P.nthreads())
+    kv = x_cpu.cuda()
+    enc = C.encode(pc, kv)
+    P.assert_same_object(P.gpu_to_np(enc), P.oracle_to_np(oenc), "encode")
+    assert enc.sizes["total_bytes"] == oenc.total_bytes
+    dec = C.decode(pc, enc)
+    assert np.array_equal(dec.cpu().numpy().view(np.uint16), odec), "decode of GPU object"
+    # decode of the oracle's object, uploaded: independent of the GPU encoder
+    dec2 = C.decode(pc, P.upload(oenc))
+    assert np.array_equal(dec2.cpu().numpy().view(np.uint16), odec), "decode of oracle object"
+    return pc, enc, oenc
+
+
+@needs_gpu
+def test_tiny_workload_bit_exact():
+    w = synth.TINY
+    _roundtrip_check(w.L, w.T, w.C, 10, 0, 1536, w.generate())
+
+
+SMALL = [
+    # L, T, C, G, chunk, tps, seed, rho, outliers
+    (2, 300, 64, 10, 128, 64, 1, 0.95, 1),      # ragged chunks and spans
+    (3, 1000, 128, 7, 333, 100, 2, 0.9, 2),     # odd group size
+    (2, 4100, 64, 10, 0, 1536, 3, 0.95, 1),     # ragged span tail in one chunk
+    (1, 1, 32, 10, 1, 1, 4, 0.9, 0),            # one token
+    (2, 57, 96, 1, 57, 20, 5, 0.9, 1),          # every token an anchor
+    (2, 31, 32, 10, 10, 10, 6, 0.5, 1),         # chunk == group
+    (1, 2000, 256, 10, 1536, 1536, 7, 0.95, 2), # full chunk + ragged chunk
+    (4, 513, 160, 3, 100, 37, 8, 0.8, 2),
+]
+
+
+@needs_gpu
+@pytest.mark.parametrize("L,T,Cc,G,chunk,tps,seed,rho,nout", SMALL)
+def test_small_shapes_bit_exact(L, T, Cc, G, chunk, tps, seed, rho, nout):
+    x = synth.ar1_kv(L, T, Cc, rho, nout, seed=seed)
+    _roundtrip_check(L, T, Cc, G, chunk, tps, x)
+
+
+@needs_gpu
+def test_escapes_and_extreme_values():
+    L, T, Cc = 2, 400, 64
+    x = synth.ar1_kv(L, T, Cc, 0.9, 2, seed=11)
+    x[0, 0, 5, 3] = 60000.0
+    x[0, 0, 6, 3] = -60000.0
+    x[1, 1, 7, 40] = 65504.0
+    x[1, 1, 8, 41] = -65504.0
+    x[0, 1, 100:110, 10] = 0.0
+    x[1, 0, :, 63] = 2.0 ** -24  # subnormal constant channel
+    _, enc, _ = _roundtrip_check(L, T, Cc, 10, 0, 128, x)
+    assert enc.sizes["n_escapes"] > 0
+    # small steps force many escapes
+    _, enc2, _ = _roundtrip_check(L, T, Cc, 10, 0, 128, synth.ar1_kv(L, T, Cc, 0.9, 2, seed=12),
+                                  step=[2.0 ** -9, 0.01])
+    assert enc2.sizes["n_escapes"] > 1000
+
+
+@needs_gpu
+def test_huge_step_and_constant_cache():
+    L, T, Cc = 2, 200, 64
+    _roundtrip_check(L, T, Cc, 10, 0, 64, synth.ar1_kv(L, T, Cc, 0.9, 1, seed=13), step=[1e6, 1e6])
+    x = torch.full((L, 2, T, Cc), 1.25, dtype=torch.float16)
+    _roundtrip_check(L, T, Cc, 10, 0, 64, x)
+    _roundtrip_check(L, T, Cc, 10, 0, 64, torch.zeros((L, 2, T, Cc), dtype=torch.float16))
+
+
+@needs_gpu
+def test_mixed_level_chunk_decode_small():
+    """Chunks of one cache taken from three encodings (step x1, x2, x4)."""
+    L, T, Cc, chunk, tps = 3, 1100, 64, 256, 100
+    x = synth.ar1_kv(L, T, Cc, 0.95, 1, seed=21)
+    x16 = x.numpy().view(np.uint16)
+    n_chunks = (T + chunk - 1) // chunk
+    levels = synth.mixed_levels(n_chunks, seed=0)
+    objs, odecs = [], []
+    for m in synth.LEVEL_MULTIPLIERS:
+        pc, oc = P.configs(L, T, Cc, 10, chunk, tps, m)
+        oenc = O.encode(oc, x16)
+        odecs.append(O.decode(oc, oenc))
+        enc = C.encode(pc, x.cuda())
+        P.assert_same_object(P.gpu_to_np(enc), P.oracle_to_np(oenc), f"level x{m}")
+        objs.append((pc, enc))
+    dst = torch.empty((L, 2, T, Cc), dtype=torch.float16, device="cuda")
+    refs = [C.ChunkRef(objs[lv][0], objs[lv][1], ch, dst, ch * chunk) for ch, lv in enumerate(levels)]
+    ws = torch.empty(C.cg_decode_chunks_ws_bytes(refs), dtype=torch.uint8, device="cuda")
+    status = C.new_status()
+    C.cg_decode_chunks(refs, ws, status)
+    torch.cuda.synchronize()
+    assert C.read_status(status) == C.CG_OK
+    got = dst.cpu().numpy().view(np.uint16)
+    for ch, lv in enumerate(levels):
+        sl = slice(ch * chunk, min(T, (ch + 1) * chunk))
+        assert np.array_equal(got[:, :, sl], odecs[lv][:, :, sl]), f"chunk {ch} level {lv}"
+    # one chunk alone into its own buffer (token offset 0)
+    one = torch.empty((L, 2, chunk, Cc), dtype=torch.float16, device="cuda")
+    ref = [C.ChunkRef(objs[2][0], objs[2][1], 1, one, 0)]
+    ws1 = torch.empty(C.cg_decode_chunks_ws_bytes(ref), dtype=torch.uint8, device="cuda")
+    C.cg_decode_chunks(ref, ws1, status)
+    torch.cuda.synchronize()
+    assert np.array_equal(one.cpu().numpy().view(np.uint16), odecs[2][:, :, chunk:2 * chunk])
+
+
+@needs_gpu
+def test_corruption_is_flagged_not_faulted():
+    L, T, Cc = 2, 700, 64
+    pc, oc = P.configs(L, T, Cc, 10, 0, 256)
+    x = synth.ar1_kv(L, T, Cc, 0.95, 1, seed=31)
+    enc = C.encode(pc, x.cuda())
+    out = torch.empty((L, 2, T, Cc), dtype=torch.float16, device="cuda")
+    cases = []
+    e1 = C.Encoded(*[getattr(enc, f).clone() for f in enc.fields()], sizes=enc.sizes)
+    e1.payload[200] ^= 0x5A                                   # flipped payload byte
+    cases.append(e1)
+    e2 = C.Encoded(*[getattr(enc, f).clone() for f in enc.fields()], sizes=enc.sizes)
+    e2.stream_off[3] += 16                                    # shifted stream boundary
+    cases.append(e2)
+    e3 = C.Encoded(*[getattr(enc, f).clone() for f in enc.fields()], sizes=enc.sizes)
+    e3.tables[3] ^= 0x01                                      # table no longer sums to 65536
+    cases.append(e3)
+    e4 = C.Encoded(*[getattr(enc, f).clone() for f in enc.fields()], sizes=enc.sizes)
+    e4.payload = e4.payload[: e4.payload.numel() // 2]        # truncated payload section
+    cases.append(e4)
+    for i, e in enumerate(cases):
+        status = C.new_status()
+        C.cg_decode(pc, e, out, status)
+        torch.cuda.synchronize()
+        assert C.read_status(status) == C.CG_ERR_CORRUPT, f"case {i}"
+    # the context is still usable
+    assert torch.equal(C.decode(pc, enc), C.decode(pc, enc))
+
+
+@needs_gpu
+def test_nonfinite_input_and_small_capacity_flagged():
+    L, T, Cc = 1, 100, 64
+    pc, _ = P.configs(L, T, Cc, 10, 0, 64)
+    x = synth.ar1_kv(L, T, Cc, 0.95, 1, seed=41).cuda()
+    x[0, 1, 17, 5] = float("nan")
+    with pytest.raises(C.CodecError) as e:
+        C.encode(pc, x)
+    assert e.value.code == C.CG_ERR_NONFINITE
+    x[0, 1, 17, 5] = float("inf")
+    with pytest.raises(C.CodecError) as e:
+        C.encode(pc, x)
+    assert e.value.code == C.CG_ERR_NONFINITE
+    # escapes capacity too small -> RANGE flagged on the device
+    y = synth.ar1_kv(L, T, Cc, 0.95, 1, seed=42)
+    y[0, 0, 1:9, :] = 1000.0
+    pc2 = C.Config(L, T, Cc, 10, T, 64, np.array([0.5], np.float32))
+    encd = C.Encoder(pc2, "cuda", escapes_cap=4)
+    encd.launch(y.cuda())
+    torch.cuda.synchronize()
+    assert C.read_status(encd.status) == C.CG_ERR_RANGE
+
+
+@needs_gpu
+def test_serialized_object_decodes_on_gpu():
+    L, T, Cc = 2, 500, 64
+    pc, oc = P.configs(L, T, Cc, 10, 200, 100)
+    x = synth.ar1_kv(L, T, Cc, 0.95, 1, seed=51)
+    enc = C.encode(pc, x.cuda())
+    buf = C.cg_serialize(pc, enc.to("cpu"))
+    cfg2, host = C.cg_deserialize(buf)
+    out = C.decode(cfg2, host.to("cuda"))
+    odec = O.decode(oc, O.encode(oc, x.numpy().view(np.uint16)))
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), odec)
+
+
+# --------------------------------------------------------------------------
+# full-size workloads, compared on whole layer ranges
+# --------------------------------------------------------------------------
+
+def _full_size_check(w: synth.Workload, layer_ranges, mult=1.0):
+    pc, _ = P.configs(w.L, w.T, w.C, 10, w.chunk_tokens, w.tokens_per_stream, mult)
+    kv = w.generate(device="cuda")
+    enc = C.encode(pc, kv)
+    dec = C.decode(pc, enc)
+    got = P.gpu_to_np(enc)
+    geo = P.Geo(w.L, w.T, w.C, 10, w.chunk_tokens, w.tokens_per_stream)
+    for l0, l1 in layer_ranges:
+        oc = O.Config(l1 - l0, w.T, w.C, 10, w.chunk_tokens or w.T, w.tokens_per_stream,
+                      O.layer_steps(w.L, mult=mult)[l0:l1])
+        x16 = kv[l0:l1].cpu().numpy().view(np.uint16)
+        oenc = O.encode(oc, x16, nthreads=P.nthreads())
+        P.assert_same_object(P.cut_layers(got, geo, l0, l1), P.oracle_to_np(oenc), f"{w.name} layers {l0}:{l1}")
+        odec = O.decode(oc, oenc, nthreads=P.nthreads())
+        assert np.array_equal(dec[l0:l1].cpu().numpy().view(np.uint16), odec), f"{w.name} decode {l0}:{l1}"
+    return pc, enc, kv
+
+
+@needs_gpu
+def test_full_size_llama70b_layer_ranges():
+    w = synth.LLAMA70B
+    _full_size_check(w, [(0, 1), (26, 28), (79, 80)])
+
+
+@needs_gpu
+def test_full_size_llama7b_layer_ranges():
+    w = synth.LLAMA7B
+    _full_size_check(w, [(0, 1), (15, 16), (31, 32)])
+
+
+@needs_gpu
+def test_full_size_mistral7b_mixed_levels():
+    w = synth.MISTRAL7B
+    kv = w.generate(device="cuda")
+    n_chunks = (w.T + w.chunk_tokens - 1) // w.chunk_tokens
+    levels = synth.mixed_levels(n_chunks, seed=0)
+    geo = P.Geo(w.L, w.T, w.C, 10, w.chunk_tokens, w.tokens_per_stream)
+    objs = []
+    for m in synth.LEVEL_MULTIPLIERS:
+        pc, _ = P.configs(w.L, w.T, w.C, 10, w.chunk_tokens, w.tokens_per_stream, m)
+        enc = C.encode(pc, kv)
+        objs.append((pc, enc, P.gpu_to_np(enc)))
+    dst = torch.empty_like(kv)
+    refs = [C.ChunkRef(objs[lv][0], objs[lv][1], ch, dst, ch * w.chunk_tokens) for ch, lv in enumerate(levels)]
+    ws = torch.empty(C.cg_decode_chunks_ws_bytes(refs), dtype=torch.uint8, device="cuda")
+    status = C.new_status()
+    C.cg_decode_chunks(refs, ws, status)
+    torch.cuda.synchronize()
+    assert C.read_status(status) == C.CG_OK
+    for l0, l1 in [(0, 1), (31, 32)]:
+        x16 = kv[l0:l1].cpu().numpy().view(np.uint16)
+        for li, m in enumerate(synth.LEVEL_MULTIPLIERS):
+            oc = O.Config(l1 - l0, w.T, w.C, 10, w.chunk_tokens, w.tokens_per_stream,
+                          O.layer_steps(w.L, mult=m)[l0:l1])
+            oenc = O.encode(oc, x16, nthreads=P.nthreads())
+            P.assert_same_object(P.cut_layers(objs[li][2], geo, l0, l1), P.oracle_to_np(oenc), f"x{m} {l0}:{l1}")
+            odec = O.decode(oc, oenc, nthreads=P.nthreads())
+            got = dst[l0:l1].cpu().numpy().view(np.uint16)
+            for ch, lv in enumerate(levels):
+                if lv != li:
+                    continue
+                sl = slice(ch * w.chunk_tokens, min(w.T, (ch + 1) * w.chunk_tokens))
+                assert np.array_equal(got[:, :, sl], odec[:, :, sl]), f"chunk {ch} x{m} layers {l0}:{l1}"
