@@ -126,12 +126,13 @@ def barrier(dist, device):
 
 def cpu_baseline(workload, seconds_hint=20.0):
     """The oracle as it stands, on a bounded sample: encode + decode of the
-    first layer of the workload (one chunk layout, all host threads)."""
+    first layers of the workload (enough (layer, K/V) slices for one thread
+    per host core, at most 8 layers)."""
     from oracle import oracle as O
     from kv_cache_compression_decode_gb300 import synth
 
     cores = os.cpu_count() or 1
-    L1 = 1
+    L1 = max(1, min(8, workload.L, cores // 2))
     x = synth.ar1_kv(L1, workload.T, workload.C, workload.rho, workload.n_outlier, workload.seed).numpy()
     oc = O.Config(L1, workload.T, workload.C, 10, workload.chunk, workload.tokens_per_stream,
                   O.layer_steps(workload.L)[:L1])
@@ -142,14 +143,14 @@ def cpu_baseline(workload, seconds_hint=20.0):
         enc = O.encode(oc, x16, nthreads=cores)
         O.decode(oc, enc, nthreads=cores)
         reps += 1
-        if time.perf_counter() - t0 > min(seconds_hint, 30.0) or reps >= 20:
+        if time.perf_counter() - t0 > min(seconds_hint, 30.0) or reps >= 5:
             break
     dt = (time.perf_counter() - t0) / reps
     gbs = x16.nbytes / dt / 1e9
     return {"value": gbs, "unit": UNIT, "cores": min(cores, 2 * L1), "kind": "oracle",
-            "sample": f"encode+decode of layer 0 (2 slices, {workload.T} tokens x {workload.C} channels, "
-                      f"{x16.nbytes / 1e6:.0f} MB fp16) of {workload.name}, {reps} reps, threads over (layer, K/V) "
-                      f"slices"}
+            "sample": f"encode+decode of layers 0..{L1 - 1} ({2 * L1} slices of {workload.T} tokens x "
+                      f"{workload.C} channels, {x16.nbytes / 1e6:.0f} MB fp16) of {workload.name}, {reps} reps, "
+                      f"one thread per (layer, K/V) slice"}
 
 
 def run_reference(args):
@@ -171,11 +172,13 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: use the first N layers of the workload (not a bench line)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -188,7 +191,11 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = synth.LLAMA70B
-    cfg = C.Config(w.L, w.T, w.C, w.group_size, w.chunk, w.tokens_per_stream, C.layer_steps(w.L))
+    if args.layers:
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}-first{args.layers}layers", L=args.layers)
+    cfg = C.Config(w.L, w.T, w.C, w.group_size, w.chunk, w.tokens_per_stream,
+                   C.layer_steps(synth.LLAMA70B.L)[: w.L])
     kv = w.generate(device=dev)
     enc = C.Encoder(cfg, dev)
     out = torch.empty_like(kv)

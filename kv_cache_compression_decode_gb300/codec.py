@@ -198,6 +198,31 @@ class Encoded:
                        self.esc_off, sizes=s)
 
 
+@dataclasses.dataclass
+class RawEncoded:
+    """An encoded object given as raw device addresses and capacities (a
+    cg_encoded as such).  Used to point the per-chunk sections at a staging
+    buffer that holds only some chunks: the section base is the staging
+    address minus the chunk range's start, so that base + offset lands in
+    the staged bytes, and the capacity is the range's end."""
+    anchors: int
+    scales: int
+    tables: int
+    table_off: int
+    payload: int
+    stream_off: int
+    escapes: int
+    esc_off: int
+    tables_cap: int
+    payload_cap: int
+    escapes_cap: int
+
+    def c(self) -> cg_encoded:
+        self._c = cg_encoded(self.anchors, self.scales, self.tables, self.table_off, self.payload, self.stream_off,
+                             self.escapes or None, self.esc_off, self.tables_cap, self.payload_cap, self.escapes_cap)
+        return self._c
+
+
 def alloc_encoded(cfg: Config, device="cuda", escapes_cap: Optional[int] = None, pin: bool = False) -> Encoded:
     """Allocate output sections for cg_encode with worst-case capacities
     (escapes default to one per 64 delta values plus 4096; cg_encode flags

@@ -38,47 +38,59 @@ _BLOCK = 64
 
 
 def _ar1_(eps: torch.Tensor, rho: float) -> torch.Tensor:
-    """AR(1) filter over dim 0 of ``eps`` [T, C] (fp32), in place semantics."""
-    T, C = eps.shape
+    """AR(1) filter over dim -2 of ``eps`` [..., T, C] (fp32)."""
+    T, C = eps.shape[-2:]
+    lead = eps.shape[:-2]
     a = math.sqrt(max(0.0, 1.0 - rho * rho))
     y = eps.clone()
     if T > 1:
-        y[1:] *= a
+        y[..., 1:, :] *= a
     nb = (T + _BLOCK - 1) // _BLOCK
     pad = nb * _BLOCK - T
     if pad:
-        y = torch.cat([y, y.new_zeros(pad, C)], 0)
+        y = torch.cat([y, y.new_zeros(*lead, pad, C)], -2)
     i = torch.arange(_BLOCK, device=eps.device, dtype=torch.float64)
     diff = i[:, None] - i[None, :]
     tri = torch.where(diff >= 0, torch.pow(torch.tensor(rho, dtype=torch.float64), diff.clamp(min=0)),
                       torch.zeros((), dtype=torch.float64))
     tri = tri.to(device=eps.device, dtype=torch.float32)
     pw = torch.pow(torch.tensor(rho, dtype=torch.float64), i + 1).to(device=eps.device, dtype=torch.float32)
-    xb = torch.matmul(tri, y.view(nb, _BLOCK, C))  # [nb, B, C]
+    xb = torch.matmul(tri, y.view(*lead, nb, _BLOCK, C))  # [..., nb, B, C]
     for b in range(1, nb):
-        xb[b] += pw[:, None] * xb[b - 1, -1][None, :]
-    return xb.reshape(nb * _BLOCK, C)[:T]
+        xb[..., b, :, :] += pw[:, None] * xb[..., b - 1, -1:, :]
+    return xb.reshape(*lead, nb * _BLOCK, C)[..., :T, :]
 
 
 def ar1_kv(L: int, T: int, C: int, rho: float, n_outlier: int, seed: int,
            device: str | torch.device = "cpu", sigma_log: float = 0.5,
            outlier_scale: float = 20.0, out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Return a seeded synthetic KV cache ``[L][2][T][C]`` fp16 on ``device``."""
+    """Return a seeded synthetic KV cache ``[L][2][T][C]`` fp16 on ``device``.
+
+    Draw order per layer: outlier permutation, then for K and V the channel
+    scales and the [T][C] normal draws.  Layers are filtered in batches so the
+    recursion runs over many layers at once."""
     dev = torch.device(device)
     g = torch.Generator(device=dev)
     g.manual_seed(int(seed))
     if out is None:
         out = torch.empty((L, 2, T, C), dtype=torch.float16, device=dev)
     assert out.shape == (L, 2, T, C) and out.dtype == torch.float16
-    for l in range(L):
-        outl = torch.randperm(C, generator=g, device=dev)[:n_outlier]
-        for kv in range(2):
-            sigma = torch.exp(torch.randn(C, generator=g, device=dev) * sigma_log)
-            if n_outlier:
-                sigma[outl] *= outlier_scale
-            eps = torch.randn((T, C), generator=g, device=dev)
-            x = _ar1_(eps, rho)
-            out[l, kv].copy_((x * sigma[None, :]).to(torch.float16))
+    batch = max(1, min(L, (1 << 28) // max(1, 2 * T * C)))  # ~1 GiB of fp32 draws per batch
+    for l0 in range(0, L, batch):
+        l1 = min(L, l0 + batch)
+        eps = torch.empty((l1 - l0, 2, T, C), dtype=torch.float32, device=dev)
+        sig = torch.empty((l1 - l0, 2, C), dtype=torch.float32, device=dev)
+        for l in range(l0, l1):
+            outl = torch.randperm(C, generator=g, device=dev)[:n_outlier]
+            for kv in range(2):
+                sigma = torch.exp(torch.randn(C, generator=g, device=dev) * sigma_log)
+                if n_outlier:
+                    sigma[outl] *= outlier_scale
+                sig[l - l0, kv] = sigma
+                eps[l - l0, kv] = torch.randn((T, C), generator=g, device=dev)
+        x = _ar1_(eps, rho)
+        out[l0:l1].copy_((x * sig[:, :, None, :]).to(torch.float16))
+        del eps, x
     return out
 
 
