@@ -34,6 +34,10 @@
  *     (1u << code): CG_ERR_NONFINITE, CG_ERR_RANGE, CG_ERR_CORRUPT,
  *     CG_ERR_TIMEOUT.  Read it after synchronizing; cg_status_from_flags()
  *     turns it into a status.  Outputs are undefined when it is non-zero.
+ *     Bits 16..22 say which check failed (diagnostics only): 16 malformed
+ *     table, 17 stream/escape offsets out of range, 18 coder end state,
+ *     19 stream length, 20 non-zero padding, 21 escape count, 22 a bounded
+ *     device wait gave up.
  *   - fp16 tensors are passed as their 16-bit patterns (uint16_t).
  *
  * Encoded object (all sections little-endian; per-chunk sections are

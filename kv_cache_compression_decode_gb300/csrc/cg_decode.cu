@@ -58,180 +58,421 @@ struct RefDst {
 };
 
 constexpr int kMaxDecWarps = 16;
+constexpr uint32_t kSegBytes = 256;                     // one bulk copy
+constexpr uint32_t kSegWords = kSegBytes / 2;           // 128 words
+constexpr uint32_t kRingSegs = 8;
+constexpr uint32_t kRingWords = kSegWords * kRingSegs;  // 1024 words = 2 KB per warp
+constexpr uint32_t kAhead = 4;                          // segments requested ahead of the one awaited
+constexpr uint32_t kMaxRun = 9;                         // steps between ring checks (<= 288 words)
+constexpr uint32_t kSpinLimit = 1u << 14;               // x 64 us suspend hint: ~1 s bound per wait
+// A run of kMaxRun steps reads at most 32 * kMaxRun words past pw; with
+// kRingSegs slots and kAhead segments requested ahead this never overwrites
+// an unread slot (see ensure()).
+static_assert(kLanes * kMaxRun <= (kRingSegs - kAhead - 1) * kSegWords + kSegWords / 4 + 32, "ring window");
 
-struct DecSmem {
-    uint32_t tab[256 * kLanes];
-    uint32_t coarse[64 * kLanes];  // bytes: [(b >> 2)][lane][b & 3]
-    uint32_t hi[kLanes];
-    float scale[kLanes];
-    int bad;
-};
+// Dynamic shared memory layout of a decode block.
+constexpr uint32_t kTabOff = 0;                              // u32 [256][32]: c | (f-1) << 16
+constexpr uint32_t kCoarseOff = kTabOff + 256 * kLanes * 4;  // u8 [(b>>2)][32][b&3]: symbol at slot 256 b
+constexpr uint32_t kDqOff = kCoarseOff + 256 * kLanes;       // f32 [256]: float(s - 127) * step
+constexpr uint32_t kHiOff = kDqOff + 256 * 4;                // u32 [32]
+constexpr uint32_t kScaleOff = kHiOff + kLanes * 4;          // f32 [32]
+constexpr uint32_t kBadOff = kScaleOff + kLanes * 4;         // int
+constexpr uint32_t kBarOff = kBadOff + 16;                   // u64 [warps][kRingSegs]
+__host__ __device__ constexpr uint32_t ring_off(uint32_t nwarps) { return kBarOff + nwarps * kRingSegs * 8; }
+__host__ __device__ constexpr uint32_t dec_smem_bytes(uint32_t nwarps) { return ring_off(nwarps) + nwarps * kRingWords * 2; }
 
-__device__ __forceinline__ uint32_t coarse_get(const DecSmem &sm, uint32_t b, uint32_t lane) {
-    return reinterpret_cast<const uint8_t *>(sm.coarse)[(((b >> 2) * kLanes + lane) << 2) | (b & 3u)];
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// 1-D bulk copy global -> shared (TMA), completion counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(65536u)
+        : "memory");
+    return ok != 0;
 }
 
-// Warp 0: build the 32 lookup tables of (slice, grp).
-__device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, DecSmem &sm, uint32_t *status) {
+// Per-warp ring of stream words, refilled 256 bytes at a time by bulk copies.
+struct Ring {
+    const uint16_t *buf;  // generic pointer to the warp's kRingWords words
+    uint32_t buf_s;       // shared address of the ring
+    uint32_t bar_s;       // shared address of bar[0] (kRingSegs consecutive u64)
+    uint32_t phase;       // bit k: parity of slot k's next completion
+};
+
+// Stream-local cursor over the ring.
+struct Cursor {
+    const uint8_t *src;  // stream start in global memory (16-byte aligned)
+    uint32_t nbytes, nw, nseg;
+    uint32_t wseg;   // next segment to wait for
+    uint32_t avail;  // words [0, avail) are in the ring
+    bool alive;
+};
+
+__device__ __forceinline__ void ring_issue(Ring &R, const Cursor &K, uint32_t k) {
+    const uint32_t off = k * kSegBytes;
+    if (k >= K.nseg) return;
+    if ((threadIdx.x & 31u) == 0) {
+        const uint32_t slot = k & (kRingSegs - 1u), bytes = min(kSegBytes, K.nbytes - off);
+        fence_proxy_async();
+        mbar_expect_tx(R.bar_s + 8u * slot, bytes);
+        bulk_g2s(R.buf_s + slot * kSegBytes, K.src + off, bytes, R.bar_s + 8u * slot);
+    }
+}
+
+// Waits (bounded) for segment k; false if the wait gave up.
+__device__ __forceinline__ bool ring_wait(Ring &R, uint32_t k) {
+    const uint32_t slot = k & (kRingSegs - 1u);
+    const uint32_t par = (R.phase >> slot) & 1u;
+    bool ok = false;
+    for (uint32_t it = 0; it < kSpinLimit && !ok; it++) ok = mbar_try_wait(R.bar_s + 8u * slot, par);
+    R.phase ^= 1u << slot;
+    return __all_sync(kFull, ok);
+}
+
+// Make words [0, need) of the stream available.  Segment k + kAhead goes
+// into the slot of segment k + kAhead - kRingSegs, which the reads have
+// passed: when segment k is awaited, pw > 128 k - 288 >= 128 (k - 3).
+__device__ __forceinline__ void ensure(Ring &R, Cursor &K, uint32_t need) {
+    while (K.avail < need && K.wseg < K.nseg) {
+        __syncwarp();
+        ring_issue(R, K, K.wseg + kAhead);
+        K.alive = ring_wait(R, K.wseg) && K.alive;
+        K.wseg++;
+        K.avail = min(K.wseg * kSegWords, K.nw);
+    }
+}
+
+__device__ __forceinline__ uint32_t coarse_at(const uint8_t *coarse, uint32_t b, uint32_t lane) {
+    return coarse[(((b >> 2) * kLanes + lane) << 2) | (b & 3u)];
+}
+
+// Warp 0: build the 32 lookup tables of (slice, grp) and the step's dequant
+// table in shared memory.
+__device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, float step, uint8_t *smem,
+                             uint32_t *status) {
     const Geom &g = o.g;
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t c = grp * kLanes + lane;
     const uint64_t table = (uint64_t)slice * g.C + c;
-    uint8_t *coarse = reinterpret_cast<uint8_t *>(sm.coarse);
+    uint32_t *tab = reinterpret_cast<uint32_t *>(smem + kTabOff);
+    uint8_t *coarse = smem + kCoarseOff;
+    float *dq = reinterpret_cast<float *>(smem + kDqOff);
+    for (uint32_t s = lane; s < 256u; s += 32u) dq[s] = __fmul_rn(__int2float_rn((int)s - 127), step);
     const uint64_t b = o.table_off[table], e = o.table_off[table + 1];
     bool ok = e >= b + 2u && e <= o.tables_cap;
     uint32_t lo = 1, hi = 0;
     if (ok) {
-        lo = o.tables[b];
-        hi = o.tables[b + 1];
+        const uint16_t h = *reinterpret_cast<const uint16_t *>(o.tables + b);
+        lo = h & 255u;
+        hi = h >> 8;
     }
+    uint32_t nb = 0;
     if (ok && lo <= hi) {
         ok = (e - b) == 2u + 2u * (hi - lo + 1u);
-        uint32_t cum = 0, nb = 0;
-        for (uint32_t s = lo; ok && s <= hi; s++) {
-            const uint64_t at = b + 2u + 2u * (s - lo);
-            const uint32_t fm1 = (uint32_t)o.tables[at] | ((uint32_t)o.tables[at + 1] << 8);
-            const uint32_t end = cum + fm1 + 1u;
-            if (end > kM) {
-                ok = false;
-                break;
+        const uint16_t *fm = reinterpret_cast<const uint16_t *>(o.tables + b + 2u);
+        uint32_t cum = 0;
+        for (uint32_t s0 = lo; ok && s0 <= hi; s0 += 8) {
+            uint32_t v[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) v[i] = s0 + i <= hi ? fm[s0 + i - lo] : 0u;  // independent loads
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                if (s0 + i > hi) break;
+                const uint32_t s = s0 + i, end = cum + v[i] + 1u;
+                if (end > kM) {
+                    ok = false;
+                    break;
+                }
+                tab[s * kLanes + lane] = cum | (v[i] << 16);
+                for (; nb < 256u && nb * 256u < end; nb++) coarse[(((nb >> 2) * kLanes + lane) << 2) | (nb & 3u)] = (uint8_t)s;
+                cum = end;
             }
-            sm.tab[s * kLanes + lane] = cum | (fm1 << 16);
-            for (; nb < 256u && nb * 256u < end; nb++) coarse[(((nb >> 2) * kLanes + lane) << 2) | (nb & 3u)] = (uint8_t)s;
-            cum = end;
         }
         ok = ok && cum == kM;
-    } else if (ok) {
-        // empty table (no delta token in this call): never looked up by a valid stream
-        for (uint32_t nb = 0; nb < 256u; nb++) coarse[(((nb >> 2) * kLanes + lane) << 2) | (nb & 3u)] = 0;
-        sm.tab[lane] = 0;
+    }
+    if (!ok || lo > hi) {
+        // empty (no delta token in this call) or invalid: any slot resolves to
+        // symbol 0 with f = 65536, and the block is skipped if invalid
+        for (; nb < 256u; nb++) coarse[(((nb >> 2) * kLanes + lane) << 2) | (nb & 3u)] = 0;
+        tab[lane] = 0xFFFF0000u;
         hi = 0;
     }
-    if (!ok) {
-        hi = 0;
-        for (uint32_t nb = 0; nb < 256u; nb++) coarse[(((nb >> 2) * kLanes + lane) << 2) | (nb & 3u)] = 0;
-        sm.tab[lane] = 0xFFFF0000u;  // f = 65536 at symbol 0: any slot resolves
-    }
-    sm.hi[lane] = hi;
-    sm.scale[lane] = o.scales[table];
+    reinterpret_cast<uint32_t *>(smem + kHiOff)[lane] = hi;
+    reinterpret_cast<float *>(smem + kScaleOff)[lane] = o.scales[table];
     const bool all_ok = __all_sync(kFull, ok);
     if (lane == 0) {
-        sm.bad = !all_ok;
-        if (!all_ok) flag(status, CG_ERR_CORRUPT);
+        *reinterpret_cast<int *>(smem + kBadOff) = !all_ok;
+        if (!all_ok) flag_why(status, CG_ERR_CORRUPT, kWhyTable);
     }
 }
 
+// Lane-private view of the block's tables.
+struct Lut {
+    const uint32_t *tab;    // this lane's column: tab[s * 32]
+    const uint8_t *coarse;
+    const float *dq;
+    uint32_t hi, lane, lt;
+};
+
+// One decode step of the lane's coder: symbol lookup, state update and the
+// warp's renormalization (lanes take the next words in lane order).
+__device__ __forceinline__ uint32_t rans_step(uint32_t &x, uint32_t &pw, const Lut &T, const uint16_t *ring) {
+    const uint32_t slot = x & 0xFFFFu;
+    uint32_t s = coarse_at(T.coarse, slot >> 8, T.lane);
+    uint32_t e = T.tab[s * kLanes];
+    uint32_t r = slot - (e & 0xFFFFu), fm1 = e >> 16;
+    if (__any_sync(kFull, r > fm1)) {  // the slot lies past the bucket's first symbol
+        while (r > fm1 && s < T.hi) {
+            s++;
+            e = T.tab[s * kLanes];
+            r = slot - (e & 0xFFFFu);
+            fm1 = e >> 16;
+        }
+    }
+    const uint32_t xh = x >> 16;
+    x = xh * fm1 + xh + r;
+    const bool need = x < kStateLow;
+    const uint32_t bal = __ballot_sync(kFull, need);
+    const uint32_t w = ring[(pw + __popc(bal & T.lt)) & (kRingWords - 1u)];
+    x = need ? __byte_perm(w, x, 0x5410) : x;  // (x << 16) | w
+    pw += __popc(bal);
+    return s;
+}
+
+template <bool kHasEsc>
+__device__ __forceinline__ float dequant(uint32_t s, const Lut &T, float step, const int32_t *escapes, uint32_t &ep,
+                                         uint32_t ee) {
+    float dq = T.dq[s];
+    if (kHasEsc) {
+        const uint32_t esb = __ballot_sync(kFull, s == kEsc);
+        if (esb) {
+            if (s == kEsc) {
+                const uint32_t idx = ep + __popc(esb & T.lt);
+                dq = __fmul_rn(__int2float_rn(idx < ee ? escapes[idx] : 0), step);
+            }
+            ep += __popc(esb);
+        }
+    }
+    return dq;
+}
+
+__device__ __forceinline__ uint16_t to_half(float v) { return __half_as_ushort(__float2half_rn(v)); }
+
 // Decode stream (slice, grp, span sp) of object o into dst (slice base).
-__device__ void decode_span(const DecObj &o, uint32_t slice, uint32_t grp, uint32_t sp, float step,
-                            const DecSmem &sm, uint16_t *dst_slice, int64_t shift, uint32_t *status) {
+// kG = 10 / kC = 1024 select compile-time group size / row stride (0: runtime).
+template <bool kHasEsc, uint32_t kG, uint32_t kC>
+__device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice, uint32_t grp, uint32_t sp,
+                                                 float step, const uint8_t *smem, Ring &R, uint16_t *dst_slice,
+                                                 int64_t shift, uint32_t *status, uint64_t sb, uint64_t se,
+                                                 uint32_t eb, uint32_t ee, uint32_t nsteps) {
     const Geom &g = o.g;
-    const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t c = grp * kLanes + lane;
-    const uint32_t lt = lanemask_lt();
+    const uint32_t G = kG ? kG : g.G;
+    const uint32_t C = kC ? kC : g.C;
+    Lut T;
+    T.lane = threadIdx.x & 31u;
+    T.lt = lanemask_lt();
+    T.tab = reinterpret_cast<const uint32_t *>(smem + kTabOff) + T.lane;
+    T.coarse = smem + kCoarseOff;
+    T.dq = reinterpret_cast<const float *>(smem + kDqOff);
+    T.hi = reinterpret_cast<const uint32_t *>(smem + kHiOff)[T.lane];
+    const uint32_t c = grp * kLanes + T.lane;
     const uint32_t ch = sp / g.spans_full, span = sp - ch * g.spans_full;
     const uint32_t c0 = ch * g.chunk, len = g.chunk_len(ch);
+    const uint32_t p0 = span * g.tps, p1 = min(p0 + g.tps, len);
+    const float sa = reinterpret_cast<const float *>(smem + kScaleOff)[T.lane];
+    const uint16_t *ring = R.buf;
+
+    Cursor K;
+    K.src = o.payload + sb;
+    K.nbytes = (uint32_t)(se - sb);
+    K.nw = K.nbytes >> 1;
+    K.nseg = (K.nbytes + kSegBytes - 1u) / kSegBytes;
+    K.wseg = 0;
+    K.avail = 0;
+    K.alive = true;
+    uint32_t x = 0, pw = 0, ep = eb;
+    if (nsteps) {
+        for (uint32_t k = 0; k < kAhead; k++) ring_issue(R, K, k);
+        ensure(R, K, 2u * kLanes);
+        x = ((uint32_t)ring[2 * T.lane] << 16) | ring[2 * T.lane + 1];
+        pw = 2u * kLanes;
+    }
+
+    uint32_t p = p0;
+    const int8_t *arow = o.anchors + g.anchor_index(slice, c0 + p0) + c;  // row of p0's group
+    uint16_t *out = dst_slice + ((int64_t)(c0 + p0) + shift) * (int64_t)C + c;
+    float xa = __fmul_rn((float)*arow, sa);
+    const uint32_t gp0 = p0 % G;
+    if (gp0) {  // head: the rest of a group whose anchor lies before the span
+        const uint32_t cnt = min(G - gp0, p1 - p);
+        for (uint32_t k = 0; k < cnt && K.alive; k++) {
+            if (k % kMaxRun == 0) ensure(R, K, pw + kLanes * min(kMaxRun, cnt - k));
+            const uint32_t s = rans_step(x, pw, T, ring);
+            out[(size_t)k * C] = to_half(__fadd_rn(xa, dequant<kHasEsc>(s, T, step, o.escapes, ep, ee)));
+        }
+        p += cnt;
+        out += (size_t)cnt * C;
+        arow += C;
+    }
+    // whole groups: anchor + G - 1 steps with one ring check
+    int8_t qa_next = p < p1 ? *arow : 0;
+    while (p + G <= p1 && K.alive) {
+        xa = __fmul_rn((float)qa_next, sa);
+        if (p + G < p1) qa_next = arow[C];  // prefetch the next group's anchor
+        out[0] = to_half(xa);
+        if (kG) ensure(R, K, pw + kLanes * (kG - 1u));  // kG - 1 <= kMaxRun
+#pragma unroll
+        for (uint32_t k = 1; k < (kG ? kG : 1u); k++) {
+            const uint32_t s = rans_step(x, pw, T, ring);
+            out[(size_t)k * C] = to_half(__fadd_rn(xa, dequant<kHasEsc>(s, T, step, o.escapes, ep, ee)));
+        }
+        if (!kG) {
+            for (uint32_t k = 1; k < G; k++) {
+                if ((k - 1u) % kMaxRun == 0) ensure(R, K, pw + kLanes * min(kMaxRun, G - k));
+                const uint32_t s = rans_step(x, pw, T, ring);
+                out[(size_t)k * C] = to_half(__fadd_rn(xa, dequant<kHasEsc>(s, T, step, o.escapes, ep, ee)));
+            }
+        }
+        p += G;
+        out += (size_t)G * C;
+        arow += C;
+    }
+    if (p < p1 && K.alive) {  // tail: a group cut by the span end
+        xa = __fmul_rn((float)qa_next, sa);
+        out[0] = to_half(xa);
+        const uint32_t cnt = p1 - p - 1u;
+        for (uint32_t k = 1; k <= cnt && K.alive; k++) {
+            if ((k - 1u) % kMaxRun == 0) ensure(R, K, pw + kLanes * min(kMaxRun, cnt - k + 1u));
+            const uint32_t s = rans_step(x, pw, T, ring);
+            out[(size_t)k * C] = to_half(__fadd_rn(xa, dequant<kHasEsc>(s, T, step, o.escapes, ep, ee)));
+        }
+    }
+    // drain copies still in flight before the ring is reused
+    for (uint32_t k = K.wseg; k < K.nseg && k < K.wseg + kAhead; k++) K.alive = ring_wait(R, k) && K.alive;
+    if (!K.alive) {
+        if (T.lane == 0) flag_why(status, CG_ERR_TIMEOUT, kWhyWait);
+        return false;
+    }
+    uint32_t why = ep == ee ? 0u : kWhyEscapes;
+    if (nsteps) {
+        if (!__all_sync(kFull, x == kStateLow)) why |= kWhyState;
+        if (!(pw <= K.nw && K.nw - pw < 8u)) why |= kWhyLength;
+        const uint16_t *wg = reinterpret_cast<const uint16_t *>(K.src);
+        bool zero = true;
+        for (uint32_t i = pw + T.lane; i < K.nw && i >= pw; i += 32) zero = zero && wg[i] == 0;
+        if (!__all_sync(kFull, zero)) why |= kWhyPadding;
+    }
+    if (why && T.lane == 0) flag_why(status, CG_ERR_CORRUPT, why);
+    return true;
+}
+
+// Returns false once a bounded wait of this warp has given up: the warp's
+// ring state is then unknown and it takes no further stream.
+__device__ bool decode_span(const DecObj &o, uint32_t slice, uint32_t grp, uint32_t sp, float step,
+                            const uint8_t *smem, Ring &R, uint16_t *dst_slice, int64_t shift, uint32_t *status) {
+    const Geom &g = o.g;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t ch = sp / g.spans_full, span = sp - ch * g.spans_full;
+    const uint32_t len = g.chunk_len(ch);
     const uint32_t p0 = span * g.tps, p1 = min(p0 + g.tps, len);
     const uint64_t k = g.stream_index(ch, slice, span, grp);
     const uint64_t sb = o.stream_off[k], se = o.stream_off[k + 1];
     const uint32_t eb = o.esc_off[k], ee = o.esc_off[k + 1];
     const uint32_t nsteps = g.steps_in(p0, p1);
     const uint64_t nw = (se - sb) >> 1;
-    bool bad = se < sb || (sb & 15u) || (se & 15u) || se > o.payload_cap || ee < eb || ee > o.escapes_cap ||
-               (nsteps == 0 && nw != 0) || (nsteps != 0 && nw < 2u * kLanes);
+    const bool bad = se < sb || (sb & 15u) || (se & 15u) || se > o.payload_cap || ee < eb || ee > o.escapes_cap ||
+                     (nsteps == 0 && nw != 0) || (nsteps != 0 && nw < 2u * kLanes) || nw > 0xFFFFFFFull;
     if (bad) {
-        if (lane == 0) flag(status, CG_ERR_CORRUPT);
-        return;
+        if (lane == 0) flag_why(status, CG_ERR_CORRUPT, kWhyOffsets);
+        return true;
     }
-    const uint16_t *w = reinterpret_cast<const uint16_t *>(o.payload + sb);
-    const float sa = sm.scale[lane];
-    const uint32_t hi = sm.hi[lane];
-    uint32_t x = nsteps ? (((uint32_t)w[2 * lane] << 16) | w[2 * lane + 1]) : 0u;
-    uint64_t pw = 2u * kLanes;
-    uint32_t ep = eb;
+#define CG_SPAN(E, GG, CC) \
+    decode_span_impl<E, GG, CC>(o, slice, grp, sp, step, smem, R, dst_slice, shift, status, sb, se, eb, ee, nsteps)
+    if (g.G == 10 && g.C == 1024) return ee != eb ? CG_SPAN(true, 10, 1024) : CG_SPAN(false, 10, 1024);
+    if (g.G == 10) return ee != eb ? CG_SPAN(true, 10, 0) : CG_SPAN(false, 10, 0);
+    return ee != eb ? CG_SPAN(true, 0, 0) : CG_SPAN(false, 0, 0);
+#undef CG_SPAN
+}
 
-    uint32_t gp = p0 % g.G;
-    const uint64_t arow0 = g.anchor_index(slice, c0 + p0);  // row of p0's group
-    int64_t aidx = (int64_t)arow0 + c - (gp == 0 ? (int64_t)g.C : 0);
-    float xa = gp ? __fmul_rn((float)o.anchors[aidx], sa) : 0.f;
-    uint16_t *out = dst_slice + ((int64_t)(c0 + p0) + shift) * (int64_t)g.C + c;
-
-    for (uint32_t p = p0; p < p1; p++, out += g.C) {
-        if (gp == 0) {
-            aidx += g.C;
-            xa = __fmul_rn((float)o.anchors[aidx], sa);
-            *out = __half_as_ushort(__float2half_rn(xa));
-        } else {
-            const uint32_t slot = x & 0xFFFFu;
-            uint32_t s = coarse_get(sm, slot >> 8, lane);
-            uint32_t e = sm.tab[s * kLanes + lane];
-            uint32_t r = slot - (e & 0xFFFFu), f = (e >> 16) + 1u;
-            while (r >= f && s < hi) {
-                s++;
-                e = sm.tab[s * kLanes + lane];
-                r = slot - (e & 0xFFFFu);
-                f = (e >> 16) + 1u;
-            }
-            x = f * (x >> 16) + r;
-            const bool need = x < kStateLow;
-            const uint32_t bal = __ballot_sync(kFull, need);
-            if (need) {
-                const uint64_t idx = pw + __popc(bal & lt);
-                x = (x << 16) | (idx < nw ? (uint32_t)w[idx] : 0u);
-            }
-            pw += __popc(bal);
-            int q = (int)s - 127;
-            const uint32_t esb = __ballot_sync(kFull, s == kEsc);
-            if (esb) {
-                if (s == kEsc) {
-                    const uint32_t idx = ep + __popc(esb & lt);
-                    q = idx < ee ? o.escapes[idx] : 0;
-                }
-                ep += __popc(esb);
-            }
-            *out = __half_as_ushort(__float2half_rn(__fadd_rn(xa, __fmul_rn(__int2float_rn(q), step))));
-        }
-        if (++gp == g.G) gp = 0;
+__device__ __forceinline__ Ring make_ring(uint8_t *smem, uint32_t nwarps) {
+    const uint32_t warp = threadIdx.x >> 5;
+    Ring R;
+    R.buf = reinterpret_cast<const uint16_t *>(smem + ring_off(nwarps)) + warp * kRingWords;
+    R.buf_s = smem_addr(R.buf);
+    R.bar_s = smem_addr(smem + kBarOff) + warp * kRingSegs * 8u;
+    R.phase = 0;
+    if ((threadIdx.x & 31u) == 0) {
+        for (uint32_t k = 0; k < kRingSegs; k++) mbar_init(R.bar_s + 8u * k);
+        fence_barrier_init();
+        fence_proxy_async();  // the initialized barriers are seen by the bulk-copy unit
     }
-    bool ok = ep == ee;
-    if (nsteps) {
-        ok = ok && __all_sync(kFull, x == kStateLow) && pw <= nw && nw - pw < 8u;
-        bool zero = true;
-        for (uint64_t i = pw + lane; i < nw; i += 32) zero = zero && w[i] == 0;
-        ok = ok && __all_sync(kFull, zero);
-    }
-    if (!ok && lane == 0) flag(status, CG_ERR_CORRUPT);
+    __syncwarp();
+    return R;
 }
 
 __global__ void __launch_bounds__(kMaxDecWarps * 32) k_decode_all(DecObj o, StepTable st, uint16_t *out,
-                                                                   uint32_t *status) {
-    __shared__ DecSmem sm;
+                                                                      uint32_t *status) {
+    extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t grp = blockIdx.x, slice = blockIdx.y, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    if (warp == 0) build_tables(o, slice, grp, sm, status);
-    __syncthreads();
-    if (sm.bad) return;
     const float step = st.v[slice >> 1];
+    Ring R = make_ring(smem, nw);
+    if (warp == 0) build_tables(o, slice, grp, step, smem, status);
+    __syncthreads();
+    if (*reinterpret_cast<const int *>(smem + kBadOff)) return;
     uint16_t *dst = out + (uint64_t)slice * o.g.T * o.g.C;
     for (uint64_t sp = warp; sp < o.g.spans_total; sp += nw)
-        decode_span(o, slice, grp, (uint32_t)sp, step, sm, dst, 0, status);
+        if (!decode_span(o, slice, grp, (uint32_t)sp, step, smem, R, dst, 0, status)) break;
 }
 
 __global__ void __launch_bounds__(kMaxDecWarps * 32) k_decode_jobs(const DecObj *objs, const DecJob *jobs,
-                                                                    const SpanRef *spans, const RefDst *refs,
-                                                                    uint32_t *status) {
-    __shared__ DecSmem sm;
+                                                                       const SpanRef *spans, const RefDst *refs,
+                                                                       uint32_t *status) {
+    extern __shared__ __align__(128) uint8_t smem[];
     const DecJob job = jobs[blockIdx.x];
     const DecObj &o = objs[job.obj];
     const uint32_t warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    if (warp == 0) build_tables(o, job.slice, job.grp, sm, status);
-    __syncthreads();
-    if (sm.bad) return;
     const float step = o.step[job.slice >> 1];
+    Ring R = make_ring(smem, nw);
+    if (warp == 0) build_tables(o, job.slice, job.grp, step, smem, status);
+    __syncthreads();
+    if (*reinterpret_cast<const int *>(smem + kBadOff)) return;
     for (uint32_t i = warp; i < job.span_count; i += nw) {
         const SpanRef sr = spans[job.span_begin + i];
         const RefDst rd = refs[sr.ref];
-        decode_span(o, job.slice, job.grp, sr.span, step, sm, rd.dst + (uint64_t)job.slice * rd.dst_tokens * o.g.C,
-                    rd.shift, status);
+        if (!decode_span(o, job.slice, job.grp, sr.span, step, smem, R,
+                         rd.dst + (uint64_t)job.slice * rd.dst_tokens * o.g.C, rd.shift, status))
+            break;
     }
+}
+
+static cudaError_t set_smem_attrs() {
+    static cudaError_t err = [] {
+        cudaError_t e = cudaFuncSetAttribute(k_decode_all, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)dec_smem_bytes(kMaxDecWarps));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_decode_jobs, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)dec_smem_bytes(kMaxDecWarps));
+        return e;
+    }();
+    return err;
 }
 
 static bool fill_obj(const cg_config *cfg, const cg_encoded *enc, DecObj *o) {
@@ -337,7 +578,9 @@ extern "C" cg_status cg_decode(const cg_config *cfg, const cg_encoded *enc, uint
     StepTable st;
     for (uint32_t l = 0; l < o.g.L; l++) st.v[l] = cfg->step[l];
     const dim3 grid(o.g.NG, o.g.n_slices);
-    k_decode_all<<<grid, warps_for(o.g.spans_total) * 32, 0, static_cast<cudaStream_t>(stream)>>>(o, st, kv_out,
+    CG_CUDA_TRY(set_smem_attrs());
+    const uint32_t nwarps = warps_for(o.g.spans_total);
+    k_decode_all<<<grid, nwarps * 32, dec_smem_bytes(nwarps), static_cast<cudaStream_t>(stream)>>>(o, st, kv_out,
                                                                                                   dev_status);
     CG_CUDA_TRY(cudaGetLastError());
     return CG_OK;
@@ -375,7 +618,9 @@ extern "C" cg_status cg_decode_chunks(const cg_chunk_ref *refs, uint32_t n, void
     // Pageable source: the copy is staged before cudaMemcpyAsync returns, so
     // `host` may be released when this function returns.
     CG_CUDA_TRY(cudaMemcpyAsync(w, host.data(), P.bytes, cudaMemcpyHostToDevice, s));
-    k_decode_jobs<<<(unsigned)P.jobs.size(), warps_for(P.max_spans) * 32, 0, s>>>(
+    CG_CUDA_TRY(set_smem_attrs());
+    const uint32_t nwarps = warps_for(P.max_spans);
+    k_decode_jobs<<<(unsigned)P.jobs.size(), nwarps * 32, dec_smem_bytes(nwarps), s>>>(
         reinterpret_cast<const DecObj *>(w + P.off_objs), reinterpret_cast<const DecJob *>(w + P.off_jobs),
         reinterpret_cast<const SpanRef *>(w + P.off_spans), reinterpret_cast<const RefDst *>(w + P.off_refs),
         dev_status);

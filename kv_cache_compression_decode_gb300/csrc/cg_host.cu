@@ -71,7 +71,7 @@ extern "C" const char *cg_status_string(cg_status s) {
 }
 
 extern "C" cg_status cg_status_from_flags(uint32_t flags) {
-    for (uint32_t c = 1; c < 32; c++)
+    for (uint32_t c = 1; c < 16; c++)  // bits 16+ are diagnostics
         if (flags & (1u << c)) return (cg_status)c;
     return CG_OK;
 }

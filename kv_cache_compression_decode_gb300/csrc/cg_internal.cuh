@@ -88,6 +88,19 @@ __device__ inline void flag(uint32_t *status, cg_status code) {
     if (status) atomicOr(status, 1u << (uint32_t)code);
 }
 
+// Diagnostic bits above the status codes: which check failed.
+constexpr uint32_t kWhyTable = 1u << 16;    // a frequency table is malformed
+constexpr uint32_t kWhyOffsets = 1u << 17;  // stream / escape offsets out of range
+constexpr uint32_t kWhyState = 1u << 18;    // a coder state did not end at 2^16
+constexpr uint32_t kWhyLength = 1u << 19;   // words consumed do not match the stream length
+constexpr uint32_t kWhyPadding = 1u << 20;  // non-zero padding after the stream
+constexpr uint32_t kWhyEscapes = 1u << 21;  // escapes consumed do not match the count
+constexpr uint32_t kWhyWait = 1u << 22;     // a bounded wait gave up
+
+__device__ inline void flag_why(uint32_t *status, cg_status code, uint32_t why) {
+    if (status) atomicOr(status, (1u << (uint32_t)code) | why);
+}
+
 __device__ inline uint32_t lanemask_lt() {
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));

@@ -56,6 +56,9 @@ SMALL = [
     (2, 31, 32, 10, 10, 10, 6, 0.5, 1),         # chunk == group
     (1, 2000, 256, 10, 1536, 1536, 7, 0.95, 2), # full chunk + ragged chunk
     (4, 513, 160, 3, 100, 37, 8, 0.8, 2),
+    (2, 900, 64, 23, 300, 250, 9, 0.95, 1),    # groups longer than a ring run
+    (1, 700, 32, 15, 700, 700, 10, 0.9, 1),
+    (2, 3000, 1024, 10, 1000, 400, 11, 0.9, 2),  # group/row fast path, ragged spans
 ]
 
 
