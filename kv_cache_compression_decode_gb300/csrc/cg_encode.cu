@@ -98,6 +98,102 @@ __device__ __forceinline__ void warp_argmax(uint32_t &v, uint32_t &s) {
 
 constexpr int kStatsWarps = 8;
 
+// Token of anchor row r (over all chunks of one slice).
+__device__ __forceinline__ uint32_t anchor_token(const Geom &g, uint32_t r) {
+    const uint32_t ch = r / g.apc_full;
+    return ch * g.chunk + (r - ch * g.apc_full) * g.G;
+}
+
+// Quantize one group's anchor and deltas and count the delta symbols.
+// v[0] is the anchor token's value, v[1..N-1] the deltas' (already loaded).
+template <uint32_t N>
+__device__ __forceinline__ void stats_full_group(const EncArgs &a, uint32_t slice, uint32_t grp, uint32_t ch,
+                                                 uint32_t c0, uint32_t p0, const float (&v)[N], float sa, float step,
+                                                 uint32_t *hist, bool &nonfinite) {
+    const Geom &g = a.g;
+    const uint32_t lane = threadIdx.x & 31u, c = grp * kLanes + lane;
+    nonfinite |= !isfinite(v[0]);
+    const float qa = fminf(fmaxf(rintf(__fdiv_rn(v[0], sa)), -127.f), 127.f);
+    a.anchors[g.anchor_index(slice, c0 + p0) + c] = (int8_t)qa;
+    const float xa = __fmul_rn(qa, sa);
+#pragma unroll
+    for (uint32_t i = 1; i < N; i++) {
+        nonfinite |= !isfinite(v[i]);
+        const int q = __float2int_rn(__fdiv_rn(__fsub_rn(v[i], xa), step));
+        const uint32_t s = symbol_of(q);
+        atomicAdd(&hist[s * kLanes + lane], 1u);
+        if (s == kEsc) atomicAdd(&a.esc_count[g.stream_index(ch, slice, (p0 + i) / g.tps, grp)], 1u);
+    }
+}
+
+// Same for a group of any length n (loads inside the loop).
+__device__ __forceinline__ void stats_any_group(const EncArgs &a, uint32_t slice, uint32_t grp, uint32_t ch, uint32_t c0,
+                                             uint32_t p0, uint32_t n, const uint16_t *x, float sa, float step,
+                                             uint32_t *hist, bool &nonfinite) {
+    const Geom &g = a.g;
+    const uint32_t lane = threadIdx.x & 31u, c = grp * kLanes + lane;
+    const uint16_t *xp = x + (uint64_t)(c0 + p0) * g.C;
+    const float v0 = ld_half(xp);
+    nonfinite |= !isfinite(v0);
+    const float qa = fminf(fmaxf(rintf(__fdiv_rn(v0, sa)), -127.f), 127.f);
+    a.anchors[g.anchor_index(slice, c0 + p0) + c] = (int8_t)qa;
+    const float xa = __fmul_rn(qa, sa);
+    for (uint32_t i = 1; i < n; i++) {
+        const float vi = ld_half(xp + (uint64_t)i * g.C);
+        nonfinite |= !isfinite(vi);
+        const int q = __float2int_rn(__fdiv_rn(__fsub_rn(vi, xa), step));
+        const uint32_t s = symbol_of(q);
+        atomicAdd(&hist[s * kLanes + lane], 1u);
+        if (s == kEsc) atomicAdd(&a.esc_count[g.stream_index(ch, slice, (p0 + i) / g.tps, grp)], 1u);
+    }
+}
+
+// All groups of one slice and channel group, warps strided over groups.
+// kG > 0: compile-time group size; two whole groups are loaded before either
+// is processed so that 2 kG row loads are in flight per lane.
+template <uint32_t kG>
+__device__ __forceinline__ void stats_groups(const EncArgs &a, uint32_t slice, uint32_t grp, const uint16_t *x,
+                                             float sa, float step, uint32_t *hist, bool &nonfinite) {
+    const Geom &g = a.g;
+    const uint32_t warp = threadIdx.x >> 5, A = (uint32_t)g.A;
+    for (uint32_t r0 = warp; r0 < A; r0 += 2u * kStatsWarps) {
+        uint32_t ch[2], c0[2], p0[2], n[2];
+        float v0[kG ? kG : 1], v1[kG ? kG : 1];
+#pragma unroll
+        for (int j = 0; j < 2; j++) {
+            const uint32_t r = r0 + (uint32_t)j * kStatsWarps;
+            n[j] = 0;
+            ch[j] = c0[j] = p0[j] = 0;
+            if (r < A) {
+                ch[j] = r / g.apc_full;
+                c0[j] = ch[j] * g.chunk;
+                p0[j] = (r - ch[j] * g.apc_full) * g.G;
+                n[j] = min(g.G, g.chunk_len(ch[j]) - p0[j]);
+            }
+        }
+        if (kG) {
+            if (n[0] == kG) {
+                const uint16_t *xp = x + (uint64_t)(c0[0] + p0[0]) * g.C;
+#pragma unroll
+                for (uint32_t i = 0; i < (kG ? kG : 1); i++) v0[i] = ld_half(xp + (uint64_t)i * g.C);
+            }
+            if (n[1] == kG) {
+                const uint16_t *xp = x + (uint64_t)(c0[1] + p0[1]) * g.C;
+#pragma unroll
+                for (uint32_t i = 0; i < (kG ? kG : 1); i++) v1[i] = ld_half(xp + (uint64_t)i * g.C);
+            }
+        }
+        if (kG && n[0] == kG)
+            stats_full_group(a, slice, grp, ch[0], c0[0], p0[0], v0, sa, step, hist, nonfinite);
+        else if (n[0])
+            stats_any_group(a, slice, grp, ch[0], c0[0], p0[0], n[0], x, sa, step, hist, nonfinite);
+        if (kG && n[1] == kG)
+            stats_full_group(a, slice, grp, ch[1], c0[1], p0[1], v1, sa, step, hist, nonfinite);
+        else if (n[1])
+            stats_any_group(a, slice, grp, ch[1], c0[1], p0[1], n[1], x, sa, step, hist, nonfinite);
+    }
+}
+
 __global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable st) {
     const Geom &g = a.g;
     const uint32_t grp = blockIdx.x, slice = blockIdx.y;
@@ -112,12 +208,20 @@ __global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable
 
     for (uint32_t i = threadIdx.x; i < 256u * kLanes; i += blockDim.x) hist[i] = 0;
 
-    // E1: absmax over this call's anchor rows -> scale = absmax / 127.
+    // E1: absmax over this call's anchor rows -> scale = absmax / 127
+    // (four independent row loads in flight per lane).
     float amax = 0.f;
-    for (uint64_t r = warp; r < g.A; r += kStatsWarps) {
-        uint32_t ch = (uint32_t)(r / g.apc_full), ar = (uint32_t)(r - (uint64_t)ch * g.apc_full);
-        uint32_t t = ch * g.chunk + ar * g.G;
-        amax = fmaxf(amax, fabsf(ld_half(x + (uint64_t)t * g.C)));
+    const uint32_t A = (uint32_t)g.A;
+    for (uint32_t r0 = warp; r0 < A; r0 += 4u * kStatsWarps) {
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const uint32_t r = r0 + (uint32_t)i * kStatsWarps;
+            v[i] = 0.f;
+            if (r < A) v[i] = ld_half(x + (uint64_t)anchor_token(g, r) * g.C);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; i++) amax = fmaxf(amax, fabsf(v[i]));
     }
     red[warp][lane] = amax;
     __syncthreads();
@@ -131,26 +235,13 @@ __global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable
     __syncthreads();
     const float sa = s_scale[lane];
 
-    // E2 + E3 + E4: one warp per group of tokens (anchor + its deltas).
+    // E2 + E3 + E4: one warp per group of tokens (anchor + its deltas); the
+    // 10-token groups of the CacheGen pipeline load two whole groups at once.
     bool nonfinite = false;
-    for (uint64_t r = warp; r < g.A; r += kStatsWarps) {
-        uint32_t ch = (uint32_t)(r / g.apc_full), ar = (uint32_t)(r - (uint64_t)ch * g.apc_full);
-        uint32_t c0 = ch * g.chunk, len = g.chunk_len(ch);
-        uint32_t p0 = ar * g.G, p1 = min(p0 + g.G, len);
-        float v = ld_half(x + (uint64_t)(c0 + p0) * g.C);
-        nonfinite |= !isfinite(v);
-        float qa = fminf(fmaxf(rintf(__fdiv_rn(v, sa)), -127.f), 127.f);
-        a.anchors[g.anchor_index(slice, c0 + p0) + c] = (int8_t)qa;
-        float xa = __fmul_rn(qa, sa);
-        for (uint32_t p = p0 + 1; p < p1; p++) {
-            v = ld_half(x + (uint64_t)(c0 + p) * g.C);
-            nonfinite |= !isfinite(v);
-            int q = __float2int_rn(__fdiv_rn(__fsub_rn(v, xa), step));
-            uint32_t s = symbol_of(q);
-            atomicAdd(&hist[s * kLanes + lane], 1u);
-            if (s == kEsc) atomicAdd(&a.esc_count[g.stream_index(ch, slice, p / g.tps, grp)], 1u);
-        }
-    }
+    if (g.G == 10)
+        stats_groups<10>(a, slice, grp, x, sa, step, hist, nonfinite);
+    else
+        stats_groups<0>(a, slice, grp, x, sa, step, hist, nonfinite);
     if (__any_sync(kFull, nonfinite) && lane == 0) flag(a.status, CG_ERR_NONFINITE);
     __syncthreads();
 
@@ -160,6 +251,7 @@ __global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable
         uint32_t n[8], f[8];
         uint32_t N = 0, lo = 256, hi = 0;
         bool any = false;
+        #pragma unroll
         for (int i = 0; i < 8; i++) {
             uint32_t s = (uint32_t)i * 32u + lane;
             n[i] = hist[s * kLanes + j];
@@ -184,6 +276,7 @@ __global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable
             continue;
         }
         uint32_t sum = 0, bn = 0, bs = 256;
+        #pragma unroll
         for (int i = 0; i < 8; i++) {
             uint32_t s = (uint32_t)i * 32u + lane;
             f[i] = 0;
@@ -201,10 +294,15 @@ __global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable
         int R = (int)kM - (int)sum;
         if (R > 0) {
             warp_argmax(bn, bs);
-            if ((bs & 31u) == lane) f[bs >> 5] += (uint32_t)R;
+            if ((bs & 31u) == lane) {
+#pragma unroll
+                for (int i = 0; i < 8; i++)
+                    if ((uint32_t)i == (bs >> 5)) f[i] += (uint32_t)R;
+            }
         }
         for (int guard = 0; R < 0 && guard < 512; guard++) {
             uint32_t bf = 0, bfs = 256;
+            #pragma unroll
             for (int i = 0; i < 8; i++)
                 if (f[i] > bf) {
                     bf = f[i];
@@ -213,9 +311,14 @@ __global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable
             warp_argmax(bf, bfs);
             int dec = min((int)bf - 1, -R);
             if (dec <= 0) break;
-            if ((bfs & 31u) == lane) f[bfs >> 5] -= (uint32_t)dec;
+            if ((bfs & 31u) == lane) {
+#pragma unroll
+                for (int i = 0; i < 8; i++)
+                    if ((uint32_t)i == (bfs >> 5)) f[i] -= (uint32_t)dec;
+            }
             R += dec;
         }
+        #pragma unroll
         for (int i = 0; i < 8; i++) {
             uint32_t s = (uint32_t)i * 32u + lane;
             if (s >= lo && s <= hi) a.ftab[table * 256u + s] = (uint16_t)(f[i] - 1u);
@@ -260,16 +363,145 @@ __global__ void __launch_bounds__(1024) k_scan(const uint32_t *in, uint64_t n, O
     }
 }
 
-constexpr int kEncWarps = 8;
+constexpr int kMaxEncWarps = 16;
 
-__global__ void __launch_bounds__(kEncWarps * 32) k_encode(EncArgs a, StepTable st) {
+// floor(x / f) and x mod f for 1 <= f <= 65536 and x < f * 2^16 (so the
+// quotient is < 2^16): a float estimate from the approximate reciprocal is
+// within one of the quotient (relative error < 2^-21), then one integer
+// correction in each direction makes it exact.
+__device__ __forceinline__ void udiv_small(uint32_t x, uint32_t f, uint32_t &q, uint32_t &r) {
+    float rf;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rf) : "f"(__uint2float_rn(f)));
+    q = __float2uint_rz(__fmul_rz(__uint2float_rz(x), rf));
+    r = x - q * f;
+    if ((int32_t)r < 0) {
+        q -= 1u;
+        r += f;
+    }
+    if (r >= f) {
+        q += 1u;
+        r -= f;
+    }
+}
+
+struct EncStream {
+    uint16_t *region;
+    uint32_t top, xs, e_top;
+    uint64_t e_base;
+    bool esc_bad;
+};
+
+// One coder step of the lane's symbol, in reverse order: emit the low half
+// of the state if coding the symbol would overflow it (the warp's emitters
+// write in lane order), then x = floor(x / f) * 2^16 + x mod f + c.
+__device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab, float v, float xa, float step,
+                                         uint32_t lane, uint32_t lt, EncStream &S) {
+    const int q = __float2int_rn(__fdiv_rn(__fsub_rn(v, xa), step));
+    const uint32_t s = symbol_of(q);
+    const uint32_t eb = __ballot_sync(kFull, s == kEsc);
+    if (eb) {
+        const uint32_t ne = __popc(eb);
+        if (ne > S.e_top) {
+            S.esc_bad = true;
+        } else {
+            if (s == kEsc) {
+                const uint64_t idx = S.e_base + S.e_top - ne + __popc(eb & lt);
+                if (idx < a.escapes_cap) a.escapes[idx] = q;
+            }
+            S.e_top -= ne;
+        }
+    }
+    const uint32_t e = etab[s * kLanes + lane];
+    const uint32_t f = (e >> 16) + 1u, cs = e & 0xFFFFu;
+    const bool emit = (S.xs >> 16) >= f;
+    const uint32_t mb = __ballot_sync(kFull, emit);
+    const uint32_t nem = __popc(mb);
+    if (emit) {
+        S.region[S.top - nem + __popc(mb & lt)] = (uint16_t)(S.xs & 0xFFFFu);
+        S.xs >>= 16;
+    }
+    S.top -= nem;
+    uint32_t qd, rd;
+    udiv_small(S.xs, f, qd, rd);
+    S.xs = (qd << 16) + rd + cs;
+}
+
+// Encode one stream: groups from the span's last to its first, each group's
+// deltas in reverse.  Whole groups (kG deltas + anchor inside the span) are
+// loaded one group ahead of the one being coded.
+template <uint32_t kG>
+__device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *etab, const uint16_t *x, uint32_t slice,
+                                            uint32_t grp, uint32_t ch, uint32_t span, float sa, float step) {
+    const Geom &g = a.g;
+    const uint32_t lane = threadIdx.x & 31u, lt = lanemask_lt();
+    const uint32_t c = grp * kLanes + lane;
+    const uint32_t G = kG ? kG : g.G;
+    constexpr uint32_t kV = kG > 1 ? kG - 1u : 1u;
+    const uint32_t c0 = ch * g.chunk, len = g.chunk_len(ch);
+    const uint32_t p0 = span * g.tps, p1 = min(p0 + g.tps, len);
+    const uint64_t k = g.stream_index(ch, slice, span, grp);
+    if (g.steps_in(p0, p1) == 0) {
+        if (lane == 0) a.words_count[k] = 0;
+        return;
+    }
+    EncStream S;
+    S.region = a.scratch + k * a.region_words;
+    S.top = (uint32_t)a.region_words;
+    S.e_top = a.esc_count[k];
+    S.e_base = a.esc_off[k];
+    S.esc_bad = false;
+    S.xs = kStateLow;
+
+    uint32_t gs = (p1 - 1u) - (p1 - 1u) % G;  // chunk position of the last group's anchor
+    float cur[kV], nxt[kV];
+    float qa_cur = 0.f, qa_nxt = 0.f;
+    auto load_group = [&](uint32_t gpos, float (&buf)[kV], float &qa) {
+        const uint16_t *xp = x + (uint64_t)(c0 + gpos + 1u) * g.C;
+#pragma unroll
+        for (uint32_t i = 0; i < kV; i++) buf[i] = ld_half(xp + (uint64_t)i * g.C);
+        qa = (float)a.anchors[g.anchor_index(slice, c0 + gpos) + c];
+    };
+    bool cur_full = kG > 1 && gs >= p0 && gs + G <= p1;
+    if (cur_full) load_group(gs, cur, qa_cur);
+    while (true) {
+        const bool has_next = gs > p0;
+        const uint32_t gn = has_next ? gs - G : 0u;
+        const bool nxt_full = kG > 1 && has_next && gn >= p0;
+        if (nxt_full) load_group(gn, nxt, qa_nxt);
+        if (cur_full) {
+            const float xa = __fmul_rn(qa_cur, sa);
+#pragma unroll
+            for (uint32_t i = kV; i-- > 0;) enc_step(a, etab, cur[i], xa, step, lane, lt, S);
+        } else {
+            const float xa = __fmul_rn((float)a.anchors[g.anchor_index(slice, c0 + gs) + c], sa);
+            const uint32_t t_lo = max(gs + 1u, p0), t_hi = min(gs + G, p1);
+            for (uint32_t t = t_hi; t-- > t_lo;) enc_step(a, etab, ld_half(x + (uint64_t)(c0 + t) * g.C), xa, step, lane, lt, S);
+        }
+        if (!has_next) break;
+        gs = gn;
+        cur_full = nxt_full;
+        qa_cur = qa_nxt;
+#pragma unroll
+        for (uint32_t i = 0; i < kV; i++) cur[i] = nxt[i];
+    }
+    S.top -= 2u * kLanes;
+    S.region[S.top + 2u * lane] = (uint16_t)(S.xs >> 16);
+    S.region[S.top + 2u * lane + 1u] = (uint16_t)(S.xs & 0xFFFFu);
+    if (lane == 0) {
+        a.words_count[k] = (uint32_t)a.region_words - S.top;
+        if (S.esc_bad || S.e_top != 0) flag(a.status, CG_ERR_CORRUPT);
+    }
+}
+
+// One block per (32-channel group, slice); one warp per stream of that
+// column (up to kMaxEncWarps, then warps take several).
+__global__ void __launch_bounds__(kMaxEncWarps * 32) k_encode(EncArgs a, StepTable st) {
     const Geom &g = a.g;
     const uint32_t grp = blockIdx.x, slice = blockIdx.y;
-    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const uint32_t c = grp * kLanes + lane;
     const uint16_t *x = a.kv + (uint64_t)slice * g.T * g.C + c;
     const float step = st.v[slice >> 1];
-    const uint32_t lt = lanemask_lt();
 
     __shared__ uint32_t etab[256 * kLanes];  // [symbol][lane]: c | (f - 1) << 16
     __shared__ float s_scale[kLanes];
@@ -298,68 +530,12 @@ __global__ void __launch_bounds__(kEncWarps * 32) k_encode(EncArgs a, StepTable 
     __syncthreads();
     const float sa = s_scale[lane];
 
-    for (uint64_t sp = warp; sp < g.spans_total; sp += kEncWarps) {
+    for (uint64_t sp = warp; sp < g.spans_total; sp += nwarps) {
         const uint32_t ch = (uint32_t)(sp / g.spans_full), span = (uint32_t)(sp - (uint64_t)ch * g.spans_full);
-        const uint32_t c0 = ch * g.chunk, len = g.chunk_len(ch);
-        const uint32_t p0 = span * g.tps, p1 = min(p0 + g.tps, len);
-        const uint64_t k = g.stream_index(ch, slice, span, grp);
-        if (g.steps_in(p0, p1) == 0) {
-            if (lane == 0) a.words_count[k] = 0;
-            continue;
-        }
-        uint16_t *region = a.scratch + k * a.region_words;
-        uint32_t top = (uint32_t)a.region_words;
-        uint32_t e_top = a.esc_count[k];
-        const uint64_t e_base = a.esc_off[k];
-        bool esc_bad = false;
-        uint32_t xs = kStateLow;
-        uint32_t gp = (p1 - 1u) % g.G;  // position in group of token p1-1
-        uint32_t row_pos = p1;          // chunk position of the anchor whose value is in xa
-        float xa = 0.f;
-        for (uint32_t p = p1; p-- > p0;) {
-            const uint32_t cur_gp = gp;
-            gp = gp == 0 ? g.G - 1u : gp - 1u;
-            if (cur_gp == 0) continue;  // anchor token: not in the stream
-            const uint32_t apos = p - cur_gp;
-            if (apos != row_pos) {
-                row_pos = apos;
-                xa = __fmul_rn((float)a.anchors[g.anchor_index(slice, c0 + apos) + c], sa);
-            }
-            const float v = ld_half(x + (uint64_t)(c0 + p) * g.C);
-            const int q = __float2int_rn(__fdiv_rn(__fsub_rn(v, xa), step));
-            const uint32_t s = symbol_of(q);
-            const uint32_t eb = __ballot_sync(kFull, s == kEsc);
-            if (eb) {
-                const uint32_t ne = __popc(eb);
-                if (ne > e_top) {
-                    esc_bad = true;
-                } else {
-                    if (s == kEsc) {
-                        uint64_t idx = e_base + e_top - ne + __popc(eb & lt);
-                        if (idx < a.escapes_cap) a.escapes[idx] = q;
-                    }
-                    e_top -= ne;
-                }
-            }
-            const uint32_t e = etab[s * kLanes + lane];
-            const uint32_t f = (e >> 16) + 1u, cs = e & 0xFFFFu;
-            const bool emit = (xs >> 16) >= f;
-            const uint32_t mb = __ballot_sync(kFull, emit);
-            const uint32_t nem = __popc(mb);
-            if (emit) {
-                region[top - nem + __popc(mb & lt)] = (uint16_t)(xs & 0xFFFFu);
-                xs >>= 16;
-            }
-            top -= nem;
-            xs = ((xs / f) << 16) + (xs % f) + cs;
-        }
-        top -= 2u * kLanes;
-        region[top + 2u * lane] = (uint16_t)(xs >> 16);
-        region[top + 2u * lane + 1u] = (uint16_t)(xs & 0xFFFFu);
-        if (lane == 0) {
-            a.words_count[k] = (uint32_t)a.region_words - top;
-            if (esc_bad || e_top != 0) flag(a.status, CG_ERR_CORRUPT);
-        }
+        if (g.G == 10)
+            encode_span<10>(a, etab, x, slice, grp, ch, span, sa, step);
+        else
+            encode_span<0>(a, etab, x, slice, grp, ch, span, sa, step);
     }
 }
 
@@ -469,7 +645,8 @@ extern "C" cg_status cg_encode(const cg_config *cfg, const uint16_t *kv, void *w
     k_stats<<<grid, kStatsWarps * 32, 0, s>>>(a, st);
     k_scan<uint32_t, false><<<1, 1024, 0, s>>>(a.twidth, g.n_tables, a.table_off, a.tables_cap, a.status);
     k_scan<uint32_t, false><<<1, 1024, 0, s>>>(a.esc_count, g.n_streams, a.esc_off, a.escapes_cap, a.status);
-    k_encode<<<grid, kEncWarps * 32, 0, s>>>(a, st);
+    const uint32_t enc_warps = (uint32_t)(g.spans_total < (uint64_t)kMaxEncWarps ? g.spans_total : kMaxEncWarps);
+    k_encode<<<grid, enc_warps * 32, 0, s>>>(a, st);
     k_scan<uint64_t, true><<<1, 1024, 0, s>>>(a.words_count, g.n_streams, a.stream_off, a.payload_cap, a.status);
     const uint64_t pack_blocks = (g.n_streams * 32u + 255u) / 256u;
     k_pack<<<(unsigned)pack_blocks, 256, 0, s>>>(a);
