@@ -200,6 +200,34 @@ cg_status cg_decode_chunks_ws_bytes(const cg_chunk_ref *refs, uint32_t n, size_t
 cg_status cg_decode_chunks(const cg_chunk_ref *refs, uint32_t n, void *ws, size_t ws_bytes, uint32_t *dev_status,
                            void *stream);
 
+/*
+ * Chunked decode for callers that cannot allocate device memory.  The CacheGen
+ * pages have no counterpart to this; it exists for users of this library.
+ *
+ * cg_decode_chunks needs a device workspace for its job descriptors.  Some
+ * callers cannot provide one: code that runs where every device byte is
+ * owned by someone else (a serving engine's pre-sized KV pool, a plugin that
+ * may not call cudaMalloc or a caching allocator), or a hot path that must not
+ * pay for allocation.  This entry point takes the same refs but keeps the
+ * descriptors in a fixed device array inside libcg, CG_NOALLOC_DESC_BYTES
+ * (4 MiB) long, which every GPU that loads the library holds until the
+ * process exits.  It calls no cudaMalloc or cudaFree and no allocating
+ * routine; the host side plans into static storage as well.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) and keeps it; make that first call before any
+ *     stream capture.
+ *   - Every call rewrites the array, so calls that overlap on the GPU race:
+ *     issue them on one stream, or order them with events.  Calls from
+ *     several host threads are serialized by a lock.
+ *   - CG_ERR_RANGE if the refs need more descriptor bytes than the array
+ *     holds (cg_decode_chunks_ws_bytes reports the need; a few hundred
+ *     objects' worth of jobs fit), CG_ERR_INVALID_ARG / CG_ERR_CUDA as for
+ *     cg_decode_chunks.  Outputs and dev_status behave as in
+ *     cg_decode_chunks.
+ */
+#define CG_NOALLOC_DESC_BYTES (4u << 20)
+cg_status cg_decode_chunks_noalloc(const cg_chunk_ref *refs, uint32_t n, uint32_t *dev_status, void *stream);
+
 /* Where chunk `chunk` lives inside the per-chunk sections: byte ranges of
  * payload and anchors, entry range of escapes, and entry ranges of
  * stream_off / esc_off that describe it.  Host only; `off` arrays are host

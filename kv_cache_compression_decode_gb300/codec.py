@@ -74,7 +74,8 @@ class cg_chunk_range(ct.Structure):
 
 # Every symbol libcg exports (the declarations of include/cg.h).
 EXPORTS = ("cg_status_string", "cg_status_from_flags", "cg_encode_bounds", "cg_encode", "cg_decode",
-           "cg_decode_chunks_ws_bytes", "cg_decode_chunks", "cg_chunk_ranges", "cg_serialize",
+           "cg_decode_chunks_ws_bytes", "cg_decode_chunks", "cg_decode_chunks_noalloc", "cg_chunk_ranges",
+           "cg_serialize",
            "cg_deserialize_header", "cg_deserialize")
 
 _lib = None
@@ -95,6 +96,7 @@ def lib() -> ct.CDLL:
         L.cg_decode.argtypes = [ct.POINTER(cg_config), ct.POINTER(cg_encoded), P, P, P]
         L.cg_decode_chunks_ws_bytes.argtypes = [ct.POINTER(cg_chunk_ref), U32, ct.POINTER(ct.c_size_t)]
         L.cg_decode_chunks.argtypes = [ct.POINTER(cg_chunk_ref), U32, P, ct.c_size_t, P, P]
+        L.cg_decode_chunks_noalloc.argtypes = [ct.POINTER(cg_chunk_ref), U32, P, P]
         L.cg_chunk_ranges.argtypes = [ct.POINTER(cg_config), U32, P, P, ct.POINTER(cg_chunk_range)]
         L.cg_serialize.argtypes = [ct.POINTER(cg_config), ct.POINTER(cg_encoded), ct.POINTER(cg_sizes), P,
                                    ct.POINTER(ct.c_size_t)]
@@ -297,6 +299,18 @@ def cg_decode_chunks(refs: Sequence[ChunkRef], ws: torch.Tensor, status: torch.T
     code = lib().cg_decode_chunks(arr, len(refs), ws.data_ptr(), ws.numel(), status.data_ptr(),
                                   _stream_ptr(stream))
     _check(code, "cg_decode_chunks")
+
+
+CG_NOALLOC_DESC_BYTES = 4 << 20
+
+
+def cg_decode_chunks_noalloc(refs: Sequence[ChunkRef], status: torch.Tensor, stream=None) -> None:
+    """cg_decode_chunks without a workspace: for callers that may not allocate
+    device memory (the descriptors go to a fixed array inside libcg; calls that
+    overlap on the GPU race, so keep them on one stream)."""
+    arr, keep = _refs(refs)
+    code = lib().cg_decode_chunks_noalloc(arr, len(refs), status.data_ptr(), _stream_ptr(stream))
+    _check(code, "cg_decode_chunks_noalloc")
 
 
 def cg_chunk_ranges(cfg: Config, chunk: int, stream_off: np.ndarray, esc_off: np.ndarray) -> dict:

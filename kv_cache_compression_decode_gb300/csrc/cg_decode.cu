@@ -19,6 +19,7 @@
 // CG_ERR_CORRUPT in the status word.
 #include <cuda_fp16.h>
 
+#include <mutex>
 #include <vector>
 
 #include "cg_internal.cuh"
@@ -623,6 +624,139 @@ extern "C" cg_status cg_decode_chunks(const cg_chunk_ref *refs, uint32_t n, void
     k_decode_jobs<<<(unsigned)P.jobs.size(), nwarps * 32, dec_smem_bytes(nwarps), s>>>(
         reinterpret_cast<const DecObj *>(w + P.off_objs), reinterpret_cast<const DecJob *>(w + P.off_jobs),
         reinterpret_cast<const SpanRef *>(w + P.off_spans), reinterpret_cast<const RefDst *>(w + P.off_refs),
+        dev_status);
+    CG_CUDA_TRY(cudaGetLastError());
+    return CG_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Chunk decode that allocates nothing: descriptors live in a file-scope
+// device array instead of a caller workspace.
+// ---------------------------------------------------------------------------
+namespace cg {
+
+// One call's descriptors (objects, destinations, span list, jobs, steps).
+static __device__ __align__(256) uint8_t g_noalloc_desc[CG_NOALLOC_DESC_BYTES];
+// Host staging for those descriptors (static storage, guarded by the mutex).
+static __align__(256) uint8_t h_noalloc_stage[CG_NOALLOC_DESC_BYTES];
+static std::mutex g_noalloc_mu;
+constexpr int kNoAllocMaxDevices = 64;
+static uint8_t *g_noalloc_dev[kNoAllocMaxDevices];  // device address of g_noalloc_desc, per device
+
+// Same descriptor layout as plan_chunks, written straight into `buf`
+// (host) for the device address `dev`, with no heap use.  Objects are the
+// distinct `enc` pointers in order of first appearance.
+struct StaticPlan {
+    uint64_t bytes, off_objs, off_refs, off_spans, off_jobs;
+    uint32_t n_jobs, max_spans;
+};
+
+static cg_status plan_chunks_static(const cg_chunk_ref *refs, uint32_t n, uint8_t *buf, size_t cap, uint8_t *dev,
+                                    StaticPlan *P) {
+    if (!refs || n == 0) return CG_ERR_INVALID_ARG;
+    auto first_of = [&](uint32_t i) {
+        uint32_t j = 0;
+        while (refs[j].enc != refs[i].enc) j++;
+        return j;
+    };
+    uint64_t n_obj = 0, n_spans = 0, jobs = 0, steps_bytes = 0;
+    for (uint32_t i = 0; i < n; i++) {
+        const cg_chunk_ref &r = refs[i];
+        DecObj o;
+        if (!fill_obj(r.cfg, r.enc, &o) || !r.dst) return CG_ERR_INVALID_ARG;
+        if (r.chunk >= o.g.n_chunks) return CG_ERR_INVALID_ARG;
+        if ((uint64_t)r.dst_token0 + o.g.chunk_len(r.chunk) > r.dst_tokens) return CG_ERR_INVALID_ARG;
+        const uint32_t f = first_of(i);
+        if (f == i) {
+            n_obj++;
+            jobs += (uint64_t)o.g.n_slices * o.g.NG;
+            steps_bytes = round_up(steps_bytes + 4ull * o.g.L, 256);
+        } else {
+            DecObj o0;
+            fill_obj(refs[f].cfg, refs[f].enc, &o0);
+            const Geom &a = o0.g, &b = o.g;
+            if (a.L != b.L || a.T != b.T || a.C != b.C || a.G != b.G || a.chunk != b.chunk || a.tps != b.tps)
+                return CG_ERR_INVALID_ARG;
+        }
+        n_spans += o.g.spc(r.chunk);
+    }
+    uint64_t o = 0;
+    auto take = [&](uint64_t nb) {
+        uint64_t at = o;
+        o = round_up(o + nb, 256);
+        return at;
+    };
+    const uint64_t off_objs = take(n_obj * sizeof(DecObj)), off_refs = take((uint64_t)n * sizeof(RefDst));
+    const uint64_t off_spans = take(n_spans * sizeof(SpanRef)), off_jobs = take(jobs * sizeof(DecJob));
+    const uint64_t off_steps = o;
+    o += steps_bytes;
+    if (o > cap || jobs > 0x7FFFFFFFull) return CG_ERR_RANGE;
+    DecObj *objs = reinterpret_cast<DecObj *>(buf + off_objs);
+    RefDst *rd = reinterpret_cast<RefDst *>(buf + off_refs);
+    SpanRef *sp = reinterpret_cast<SpanRef *>(buf + off_spans);
+    DecJob *jb = reinterpret_cast<DecJob *>(buf + off_jobs);
+    uint64_t so = off_steps, si = 0, ji = 0;
+    uint32_t k = 0, mx = 1;
+    for (uint32_t i = 0; i < n; i++) {
+        const cg_chunk_ref &r = refs[i];
+        DecObj ob;
+        fill_obj(r.cfg, r.enc, &ob);
+        rd[i].dst = r.dst;
+        rd[i].dst_tokens = r.dst_tokens;
+        rd[i].shift = (int64_t)r.dst_token0 - (int64_t)r.chunk * ob.g.chunk;
+        if (first_of(i) != i) continue;
+        // object k: its steps, its span list (all refs sharing this enc), its jobs
+        ob.step = reinterpret_cast<const float *>(dev + so);
+        memcpy(buf + so, r.cfg->step, 4ull * r.cfg->L);
+        so = round_up(so + 4ull * r.cfg->L, 256);
+        objs[k] = ob;
+        const uint32_t sb = (uint32_t)si;
+        for (uint32_t m = i; m < n; m++) {
+            if (refs[m].enc != r.enc) continue;
+            for (uint32_t q = 0; q < ob.g.spc(refs[m].chunk); q++) sp[si++] = SpanRef{refs[m].chunk * ob.g.spans_full + q, m};
+        }
+        const uint32_t cnt = (uint32_t)si - sb;
+        mx = cnt > mx ? cnt : mx;
+        for (uint32_t slice = 0; slice < ob.g.n_slices; slice++)
+            for (uint32_t grp = 0; grp < ob.g.NG; grp++) jb[ji++] = DecJob{k, slice, grp, sb, cnt};
+        k++;
+    }
+    P->bytes = o;
+    P->off_objs = off_objs;
+    P->off_refs = off_refs;
+    P->off_spans = off_spans;
+    P->off_jobs = off_jobs;
+    P->n_jobs = (uint32_t)jobs;
+    P->max_spans = mx;
+    return CG_OK;
+}
+
+}  // namespace cg
+
+extern "C" cg_status cg_decode_chunks_noalloc(const cg_chunk_ref *refs, uint32_t n, uint32_t *dev_status,
+                                              void *stream) {
+    int dev = 0;
+    CG_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return CG_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_dev[dev]) {  // first call on this device: find the array's device address
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_desc) != cudaSuccess || !p) return CG_ERR_CUDA;
+        g_noalloc_dev[dev] = static_cast<uint8_t *>(p);
+    }
+    uint8_t *d = g_noalloc_dev[dev];
+    StaticPlan P;
+    cg_status st = plan_chunks_static(refs, n, h_noalloc_stage, sizeof(h_noalloc_stage), d, &P);
+    if (st != CG_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Pageable source: staged before cudaMemcpyAsync returns, so the static
+    // host buffer is free again when the lock is released.
+    CG_CUDA_TRY(cudaMemcpyAsync(d, h_noalloc_stage, P.bytes, cudaMemcpyHostToDevice, s));
+    CG_CUDA_TRY(set_smem_attrs());
+    const uint32_t nwarps = warps_for(P.max_spans);
+    k_decode_jobs<<<P.n_jobs, nwarps * 32, dec_smem_bytes(nwarps), s>>>(
+        reinterpret_cast<const DecObj *>(d + P.off_objs), reinterpret_cast<const DecJob *>(d + P.off_jobs),
+        reinterpret_cast<const SpanRef *>(d + P.off_spans), reinterpret_cast<const RefDst *>(d + P.off_refs),
         dev_status);
     CG_CUDA_TRY(cudaGetLastError());
     return CG_OK;
