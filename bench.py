@@ -34,6 +34,10 @@ import torch  # noqa: E402
 METRIC = "cg_decode / cg_encode GB/s of fp16 KV (1xGB300, % HBM roofline); bits/value"
 UNIT = "GB/s"
 KERNELS_PER_STEP = 8  # k_stats, 3 x k_scan, k_encode, k_pack, k_sizes, k_decode_all
+# DRAM bytes (read + write) of one k_decode_all launch on the full Llama-70B
+# workload: ncu capture of the first 8 layers (603.6 MB, grows with layers)
+# scaled by 80/8.  Must be reset to None whenever k_decode_all changes.
+DECODE_TRAFFIC_BYTES = 603.6e6 * 10
 
 
 def peaks():
@@ -298,7 +302,9 @@ def main():
             "compressed_bytes": comp_bytes,
             "roofline": {"bound": "hbm", "kernel": "k_decode_all", "achieved": round(dec_achieved, 1),
                          "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "unit": "GB/s",
-                         "frac": round(dec_achieved / peak, 4), "traffic": None,
+                         "frac": round(dec_achieved / peak, 4),
+                         "traffic": (DECODE_TRAFFIC_BYTES if not args.layers else None),
+                         "traffic_source": "ncu dram__bytes_read+write of an 8-layer launch x 10",
                          "algorithmic_bytes": dec_alg},
             "encode_roofline": {"bound": "hbm", "achieved": round(enc_achieved, 1), "peak": peak, "unit": "GB/s",
                                 "frac": round(enc_achieved / peak, 4)},
