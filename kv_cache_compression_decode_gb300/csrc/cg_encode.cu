@@ -4,7 +4,8 @@
 // quantization, arithmetic coding with per-(layer, channel) statistics;
 // "CacheGen vs 传统量化KV缓存压缩技术深度对比与性能测试", §1 and §2.1):
 //   k_stats   one block per (32-channel group, layer, K/V): anchor absmax ->
-//             scale, int8 anchors, delta quantization, shared-memory
+//             scale, int8 anchors, delta quantization (multiplication by the
+//             once-rounded inverse of the scale / step), shared-memory
 //             histograms (lane = channel, bank = lane: conflict-free
 //             atomics), escape counts per stream, normalization of the 32
 //             histograms to 16-bit frequency tables (warp-cooperative).
@@ -108,18 +109,18 @@ __device__ __forceinline__ uint32_t anchor_token(const Geom &g, uint32_t r) {
 // v[0] is the anchor token's value, v[1..N-1] the deltas' (already loaded).
 template <uint32_t N>
 __device__ __forceinline__ void stats_full_group(const EncArgs &a, uint32_t slice, uint32_t grp, uint32_t ch,
-                                                 uint32_t c0, uint32_t p0, const float (&v)[N], float sa, float step,
-                                                 uint32_t *hist, bool &nonfinite) {
+                                                 uint32_t c0, uint32_t p0, const float (&v)[N], float sa, float inv_sa,
+                                                 float inv_step, uint32_t *hist, bool &nonfinite) {
     const Geom &g = a.g;
     const uint32_t lane = threadIdx.x & 31u, c = grp * kLanes + lane;
     nonfinite |= !isfinite(v[0]);
-    const float qa = fminf(fmaxf(rintf(__fdiv_rn(v[0], sa)), -127.f), 127.f);
+    const float qa = fminf(fmaxf(rintf(__fmul_rn(v[0], inv_sa)), -127.f), 127.f);
     a.anchors[g.anchor_index(slice, c0 + p0) + c] = (int8_t)qa;
     const float xa = __fmul_rn(qa, sa);
 #pragma unroll
     for (uint32_t i = 1; i < N; i++) {
         nonfinite |= !isfinite(v[i]);
-        const int q = __float2int_rn(__fdiv_rn(__fsub_rn(v[i], xa), step));
+        const int q = __float2int_rn(__fmul_rn(__fsub_rn(v[i], xa), inv_step));
         const uint32_t s = symbol_of(q);
         atomicAdd(&hist[s * kLanes + lane], 1u);
         if (s == kEsc) atomicAdd(&a.esc_count[g.stream_index(ch, slice, (p0 + i) / g.tps, grp)], 1u);
@@ -128,20 +129,20 @@ __device__ __forceinline__ void stats_full_group(const EncArgs &a, uint32_t slic
 
 // Same for a group of any length n (loads inside the loop).
 __device__ __forceinline__ void stats_any_group(const EncArgs &a, uint32_t slice, uint32_t grp, uint32_t ch, uint32_t c0,
-                                             uint32_t p0, uint32_t n, const uint16_t *x, float sa, float step,
-                                             uint32_t *hist, bool &nonfinite) {
+                                             uint32_t p0, uint32_t n, const uint16_t *x, float sa, float inv_sa,
+                                             float inv_step, uint32_t *hist, bool &nonfinite) {
     const Geom &g = a.g;
     const uint32_t lane = threadIdx.x & 31u, c = grp * kLanes + lane;
     const uint16_t *xp = x + (uint64_t)(c0 + p0) * g.C;
     const float v0 = ld_half(xp);
     nonfinite |= !isfinite(v0);
-    const float qa = fminf(fmaxf(rintf(__fdiv_rn(v0, sa)), -127.f), 127.f);
+    const float qa = fminf(fmaxf(rintf(__fmul_rn(v0, inv_sa)), -127.f), 127.f);
     a.anchors[g.anchor_index(slice, c0 + p0) + c] = (int8_t)qa;
     const float xa = __fmul_rn(qa, sa);
     for (uint32_t i = 1; i < n; i++) {
         const float vi = ld_half(xp + (uint64_t)i * g.C);
         nonfinite |= !isfinite(vi);
-        const int q = __float2int_rn(__fdiv_rn(__fsub_rn(vi, xa), step));
+        const int q = __float2int_rn(__fmul_rn(__fsub_rn(vi, xa), inv_step));
         const uint32_t s = symbol_of(q);
         atomicAdd(&hist[s * kLanes + lane], 1u);
         if (s == kEsc) atomicAdd(&a.esc_count[g.stream_index(ch, slice, (p0 + i) / g.tps, grp)], 1u);
@@ -153,7 +154,8 @@ __device__ __forceinline__ void stats_any_group(const EncArgs &a, uint32_t slice
 // is processed so that 2 kG row loads are in flight per lane.
 template <uint32_t kG>
 __device__ __forceinline__ void stats_groups(const EncArgs &a, uint32_t slice, uint32_t grp, const uint16_t *x,
-                                             float sa, float step, uint32_t *hist, bool &nonfinite) {
+                                             float sa, float inv_sa, float inv_step, uint32_t *hist,
+                                             bool &nonfinite) {
     const Geom &g = a.g;
     const uint32_t warp = threadIdx.x >> 5, A = (uint32_t)g.A;
     for (uint32_t r0 = warp; r0 < A; r0 += 2u * kStatsWarps) {
@@ -184,13 +186,13 @@ __device__ __forceinline__ void stats_groups(const EncArgs &a, uint32_t slice, u
             }
         }
         if (kG && n[0] == kG)
-            stats_full_group(a, slice, grp, ch[0], c0[0], p0[0], v0, sa, step, hist, nonfinite);
+            stats_full_group(a, slice, grp, ch[0], c0[0], p0[0], v0, sa, inv_sa, inv_step, hist, nonfinite);
         else if (n[0])
-            stats_any_group(a, slice, grp, ch[0], c0[0], p0[0], n[0], x, sa, step, hist, nonfinite);
+            stats_any_group(a, slice, grp, ch[0], c0[0], p0[0], n[0], x, sa, inv_sa, inv_step, hist, nonfinite);
         if (kG && n[1] == kG)
-            stats_full_group(a, slice, grp, ch[1], c0[1], p0[1], v1, sa, step, hist, nonfinite);
+            stats_full_group(a, slice, grp, ch[1], c0[1], p0[1], v1, sa, inv_sa, inv_step, hist, nonfinite);
         else if (n[1])
-            stats_any_group(a, slice, grp, ch[1], c0[1], p0[1], n[1], x, sa, step, hist, nonfinite);
+            stats_any_group(a, slice, grp, ch[1], c0[1], p0[1], n[1], x, sa, inv_sa, inv_step, hist, nonfinite);
     }
 }
 
@@ -238,10 +240,11 @@ __global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable
     // E2 + E3 + E4: one warp per group of tokens (anchor + its deltas); the
     // 10-token groups of the CacheGen pipeline load two whole groups at once.
     bool nonfinite = false;
+    const float inv_sa = __fdiv_rn(1.f, sa), inv_step = __fdiv_rn(1.f, step);  // one rounding each
     if (g.G == 10)
-        stats_groups<10>(a, slice, grp, x, sa, step, hist, nonfinite);
+        stats_groups<10>(a, slice, grp, x, sa, inv_sa, inv_step, hist, nonfinite);
     else
-        stats_groups<0>(a, slice, grp, x, sa, step, hist, nonfinite);
+        stats_groups<0>(a, slice, grp, x, sa, inv_sa, inv_step, hist, nonfinite);
     if (__any_sync(kFull, nonfinite) && lane == 0) flag(a.status, CG_ERR_NONFINITE);
     __syncthreads();
 
@@ -363,7 +366,7 @@ __global__ void __launch_bounds__(1024) k_scan(const uint32_t *in, uint64_t n, O
     }
 }
 
-constexpr int kMaxEncWarps = 16;
+constexpr int kMaxEncWarps = 12;
 
 // floor(x / f) and x mod f for 1 <= f <= 65536 and x < f * 2^16 (so the
 // quotient is < 2^16): a float estimate from the approximate reciprocal is
@@ -394,9 +397,9 @@ struct EncStream {
 // One coder step of the lane's symbol, in reverse order: emit the low half
 // of the state if coding the symbol would overflow it (the warp's emitters
 // write in lane order), then x = floor(x / f) * 2^16 + x mod f + c.
-__device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab, float v, float xa, float step,
+__device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab, float v, float xa, float inv_step,
                                          uint32_t lane, uint32_t lt, EncStream &S) {
-    const int q = __float2int_rn(__fdiv_rn(__fsub_rn(v, xa), step));
+    const int q = __float2int_rn(__fmul_rn(__fsub_rn(v, xa), inv_step));
     const uint32_t s = symbol_of(q);
     const uint32_t eb = __ballot_sync(kFull, s == kEsc);
     if (eb) {
@@ -431,7 +434,7 @@ __device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab,
 // loaded one group ahead of the one being coded.
 template <uint32_t kG>
 __device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *etab, const uint16_t *x, uint32_t slice,
-                                            uint32_t grp, uint32_t ch, uint32_t span, float sa, float step) {
+                                            uint32_t grp, uint32_t ch, uint32_t span, float sa, float inv_step) {
     const Geom &g = a.g;
     const uint32_t lane = threadIdx.x & 31u, lt = lanemask_lt();
     const uint32_t c = grp * kLanes + lane;
@@ -471,11 +474,11 @@ __device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *et
         if (cur_full) {
             const float xa = __fmul_rn(qa_cur, sa);
 #pragma unroll
-            for (uint32_t i = kV; i-- > 0;) enc_step(a, etab, cur[i], xa, step, lane, lt, S);
+            for (uint32_t i = kV; i-- > 0;) enc_step(a, etab, cur[i], xa, inv_step, lane, lt, S);
         } else {
             const float xa = __fmul_rn((float)a.anchors[g.anchor_index(slice, c0 + gs) + c], sa);
             const uint32_t t_lo = max(gs + 1u, p0), t_hi = min(gs + G, p1);
-            for (uint32_t t = t_hi; t-- > t_lo;) enc_step(a, etab, ld_half(x + (uint64_t)(c0 + t) * g.C), xa, step, lane, lt, S);
+            for (uint32_t t = t_hi; t-- > t_lo;) enc_step(a, etab, ld_half(x + (uint64_t)(c0 + t) * g.C), xa, inv_step, lane, lt, S);
         }
         if (!has_next) break;
         gs = gn;
@@ -495,7 +498,7 @@ __device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *et
 
 // One block per (32-channel group, slice); one warp per stream of that
 // column (up to kMaxEncWarps, then warps take several).
-__global__ void __launch_bounds__(kMaxEncWarps * 32) k_encode(EncArgs a, StepTable st) {
+__global__ void __launch_bounds__(kMaxEncWarps * 32, 3) k_encode(EncArgs a, StepTable st) {
     const Geom &g = a.g;
     const uint32_t grp = blockIdx.x, slice = blockIdx.y;
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -529,13 +532,14 @@ __global__ void __launch_bounds__(kMaxEncWarps * 32) k_encode(EncArgs a, StepTab
     }
     __syncthreads();
     const float sa = s_scale[lane];
+    const float inv_step = __fdiv_rn(1.f, step);  // the quantizer multiplies by this rounded inverse
 
     for (uint64_t sp = warp; sp < g.spans_total; sp += nwarps) {
         const uint32_t ch = (uint32_t)(sp / g.spans_full), span = (uint32_t)(sp - (uint64_t)ch * g.spans_full);
         if (g.G == 10)
-            encode_span<10>(a, etab, x, slice, grp, ch, span, sa, step);
+            encode_span<10>(a, etab, x, slice, grp, ch, span, sa, inv_step);
         else
-            encode_span<0>(a, etab, x, slice, grp, ch, span, sa, step);
+            encode_span<0>(a, etab, x, slice, grp, ch, span, sa, inv_step);
     }
 }
 

@@ -28,11 +28,13 @@
  * design notes of the repository):
  *  R1 anchor: symmetric int8, one fp32 scale per (layer, K/V, channel) over
  *     all anchor rows of the call, s = absmax / 127 (1.0 when absmax is 0),
- *     q_a = clamp(rint(x / s), -127, 127); stored raw, not entropy coded.
+ *     q_a = clamp(rint(x * (1 / s)), -127, 127); stored raw, not entropy
+ *     coded.
  *  R2 deltas are taken against the reconstructed anchor q_a * s (fp32).
- *  R3 q = rint((x - xa) / step) in fp32, round half to even; symbol q + 127
- *     when |q| <= 127, else the escape symbol 255 with q sent in an int32
- *     side array.
+ *  R3 q = rint((x - xa) * (1 / step)) in fp32, round half to even, with the
+ *     reciprocal 1 / step rounded once per layer (a uniform quantizer
+ *     multiplies by the inverse step); symbol q + 127 when |q| <= 127, else
+ *     the escape symbol 255 with q sent in an int32 side array.
  *  R4 reconstruction: fp16_rn(xa + float(q) * step); anchors fp16_rn(q_a*s).
  *     Every fp32 operation is separately rounded (no fused multiply-add).
  *  R5 tables: counts per (layer, K/V, channel) over the call, normalized to
@@ -285,9 +287,9 @@ static int slice_anchor_scales(const cgo_config *cfg, const uint16_t *x, float *
 /* Stages E2 + E3: anchor quantization, delta quantization  (R1-R3)          */
 /* ------------------------------------------------------------------------ */
 
-static int8_t quantize_anchor(float v, float s)
+static int8_t quantize_anchor(float v, float inv_s)
 {
-    float r = rintf(v / s);
+    float r = rintf(v * inv_s);
     if (r > 127.0f) r = 127.0f;
     if (r < -127.0f) r = -127.0f;
     return (int8_t)r;
@@ -297,19 +299,19 @@ static int8_t quantize_anchor(float v, float s)
 static void slice_quantize(const cgo_config *cfg, const geom *g, uint32_t l, const uint16_t *x,
                            const float *scales, int8_t *anchors, int32_t *q)
 {
-    const float step = cfg->step[l];
+    const float inv_step = 1.0f / cfg->step[l];
     for (uint32_t t = 0; t < cfg->T; t++) {
         uint32_t row = anchor_row(cfg, g, t);
         for (uint32_t c = 0; c < cfg->C; c++) {
             uint64_t i = (uint64_t)t * cfg->C + c;
             float v = cgo_f16_to_f32(x[i]);
             if (is_anchor(cfg, t)) {
-                anchors[(uint64_t)row * cfg->C + c] = quantize_anchor(v, scales[c]);
+                anchors[(uint64_t)row * cfg->C + c] = quantize_anchor(v, 1.0f / scales[c]);
                 q[i] = 0;
             } else {
                 float xa = (float)anchors[(uint64_t)row * cfg->C + c] * scales[c];
                 float d = v - xa;
-                q[i] = (int32_t)rintf(d / step);
+                q[i] = (int32_t)rintf(d * inv_step);
             }
         }
     }
