@@ -37,7 +37,7 @@ KERNELS_PER_STEP = 8  # k_stats, 3 x k_scan, k_encode, k_pack, k_sizes, k_decode
 # DRAM bytes (read + write) of one k_decode_all launch on the full Llama-70B
 # workload: ncu capture of the first 8 layers (603.6 MB, grows with layers)
 # scaled by 80/8.  Must be reset to None whenever k_decode_all changes.
-DECODE_TRAFFIC_BYTES = 603.6e6 * 10
+DECODE_TRAFFIC_BYTES = None
 
 
 def peaks():
@@ -303,7 +303,7 @@ def main():
             "roofline": {"bound": "hbm", "kernel": "k_decode_all", "achieved": round(dec_achieved, 1),
                          "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "unit": "GB/s",
                          "frac": round(dec_achieved / peak, 4),
-                         "traffic": (DECODE_TRAFFIC_BYTES if not args.layers else None),
+                         "traffic": (DECODE_TRAFFIC_BYTES if not args.layers and DECODE_TRAFFIC_BYTES else None),
                          "traffic_source": "ncu dram__bytes_read+write of an 8-layer launch x 10",
                          "algorithmic_bytes": dec_alg},
             "encode_roofline": {"bound": "hbm", "achieved": round(enc_achieved, 1), "peak": peak, "unit": "GB/s",

@@ -2,12 +2,16 @@
 //
 // One thread block per (object, layer, K/V, 32-channel group).  Warp 0 turns
 // the block's 32 compact frequency tables into shared-memory lookup tables,
-// both laid out [entry][lane] so that lane i always hits bank i:
+// laid out [entry][lane]:
 //   tab    [256][32] u32   c_s | (f_s - 1) << 16
-//   coarse [256][32] u8    symbol holding slot 256*b (bucket b of the slot)
+//   coarse [256][32] u16   bucket b (slots 256 b .. 256 b + 255): s0 << 8 | d,
+//                          s0 the symbol holding slot 256 b, d = 256 (b + 1) -
+//                          (end of s0) when s0 ends inside the bucket, else 0
 // Then every warp decodes whole streams (lane = channel): per step the lane
-// looks up its symbol (coarse bucket + a forward walk over the few symbols
-// that share the bucket), updates its 32-bit range-ANS state, and the warp
+// finds its symbol as (coarse + (slot & 255)) >> 8 -- the carry out of the low
+// byte steps past s0 exactly when the slot lies beyond s0's end -- and walks on
+// only in the rare bucket that holds two or more symbol ends (about 0.1% of
+// slots); it then updates its 32-bit range-ANS state, and the warp
 // renormalizes with one ballot (lanes take the next words in lane order).
 // Dequantization and the anchor add happen in fp32 and the fp16 result is
 // stored straight into the [L][2][T][C] layout.  This is the GPU decoder of
@@ -73,8 +77,8 @@ static_assert(kLanes * kMaxRun <= (kRingSegs - kAhead - 1) * kSegWords + kSegWor
 
 // Dynamic shared memory layout of a decode block.
 constexpr uint32_t kTabOff = 0;                              // u32 [256][32]: c | (f-1) << 16
-constexpr uint32_t kCoarseOff = kTabOff + 256 * kLanes * 4;  // u8 [(b>>2)][32][b&3]: symbol at slot 256 b
-constexpr uint32_t kDqOff = kCoarseOff + 256 * kLanes;       // f32 [256]: float(s - 127) * step
+constexpr uint32_t kCoarseOff = kTabOff + 256 * kLanes * 4;  // u16 [256][32]: s0 << 8 | d (see top)
+constexpr uint32_t kDqOff = kCoarseOff + 256 * kLanes * 2;   // f32 [256]: float(s - 127) * step
 constexpr uint32_t kHiOff = kDqOff + 256 * 4;                // u32 [32]
 constexpr uint32_t kScaleOff = kHiOff + kLanes * 4;          // f32 [32]
 constexpr uint32_t kBadOff = kScaleOff + kLanes * 4;         // int
@@ -161,9 +165,6 @@ __device__ __forceinline__ void ensure(Ring &R, Cursor &K, uint32_t need) {
     }
 }
 
-__device__ __forceinline__ uint32_t coarse_at(const uint8_t *coarse, uint32_t b, uint32_t lane) {
-    return coarse[(((b >> 2) * kLanes + lane) << 2) | (b & 3u)];
-}
 
 // Warp 0: build the 32 lookup tables of (slice, grp) and the step's dequant
 // table in shared memory.
@@ -174,7 +175,7 @@ __device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, floa
     const uint32_t c = grp * kLanes + lane;
     const uint64_t table = (uint64_t)slice * g.C + c;
     uint32_t *tab = reinterpret_cast<uint32_t *>(smem + kTabOff);
-    uint8_t *coarse = smem + kCoarseOff;
+    uint16_t *coarse = reinterpret_cast<uint16_t *>(smem + kCoarseOff) + lane;
     float *dq = reinterpret_cast<float *>(smem + kDqOff);
     for (uint32_t s = lane; s < 256u; s += 32u) dq[s] = __fmul_rn(__int2float_rn((int)s - 127), step);
     const uint64_t b = o.table_off[table], e = o.table_off[table + 1];
@@ -203,7 +204,10 @@ __device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, floa
                     break;
                 }
                 tab[s * kLanes + lane] = cum | (v[i] << 16);
-                for (; nb < 256u && nb * 256u < end; nb++) coarse[(((nb >> 2) * kLanes + lane) << 2) | (nb & 3u)] = (uint8_t)s;
+                for (; nb < 256u && nb * 256u < end; nb++) {
+                    const uint32_t bend = (nb + 1u) * 256u;
+                    coarse[nb * kLanes] = (uint16_t)(s << 8 | (end < bend ? bend - end : 0u));
+                }
                 cum = end;
             }
         }
@@ -212,7 +216,7 @@ __device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, floa
     if (!ok || lo > hi) {
         // empty (no delta token in this call) or invalid: any slot resolves to
         // symbol 0 with f = 65536, and the block is skipped if invalid
-        for (; nb < 256u; nb++) coarse[(((nb >> 2) * kLanes + lane) << 2) | (nb & 3u)] = 0;
+        for (; nb < 256u; nb++) coarse[nb * kLanes] = 0;
         tab[lane] = 0xFFFF0000u;
         hi = 0;
     }
@@ -227,8 +231,8 @@ __device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, floa
 
 // Lane-private view of the block's tables.
 struct Lut {
-    const uint32_t *tab;    // this lane's column: tab[s * 32]
-    const uint8_t *coarse;
+    const uint32_t *tab;     // this lane's column: tab[s * 32]
+    const uint16_t *coarse;  // this lane's column: coarse[b * 32]
     const float *dq;
     uint32_t hi, lane, lt;
 };
@@ -237,10 +241,11 @@ struct Lut {
 // warp's renormalization (lanes take the next words in lane order).
 __device__ __forceinline__ uint32_t rans_step(uint32_t &x, uint32_t &pw, const Lut &T, const uint16_t *ring) {
     const uint32_t slot = x & 0xFFFFu;
-    uint32_t s = coarse_at(T.coarse, slot >> 8, T.lane);
+    const uint32_t e0 = T.coarse[(slot >> 8) * kLanes];
+    uint32_t s = (e0 + (x & 0xFFu)) >> 8;
     uint32_t e = T.tab[s * kLanes];
     uint32_t r = slot - (e & 0xFFFFu), fm1 = e >> 16;
-    if (__any_sync(kFull, r > fm1)) {  // the slot lies past the bucket's first symbol
+    if (__any_sync(kFull, r > fm1)) {  // the slot lies past a second end inside its bucket
         while (r > fm1 && s < T.hi) {
             s++;
             e = T.tab[s * kLanes];
@@ -291,7 +296,7 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
     T.lane = threadIdx.x & 31u;
     T.lt = lanemask_lt();
     T.tab = reinterpret_cast<const uint32_t *>(smem + kTabOff) + T.lane;
-    T.coarse = smem + kCoarseOff;
+    T.coarse = reinterpret_cast<const uint16_t *>(smem + kCoarseOff) + T.lane;
     T.dq = reinterpret_cast<const float *>(smem + kDqOff);
     T.hi = reinterpret_cast<const uint32_t *>(smem + kHiOff)[T.lane];
     const uint32_t c = grp * kLanes + T.lane;
