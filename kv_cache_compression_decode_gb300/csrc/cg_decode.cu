@@ -237,22 +237,11 @@ struct Lut {
     uint32_t hi, lane, lt;
 };
 
-// One decode step of the lane's coder: symbol lookup, state update and the
-// warp's renormalization (lanes take the next words in lane order).
-__device__ __forceinline__ uint32_t rans_step(uint32_t &x, uint32_t &pw, const Lut &T, const uint16_t *ring) {
-    const uint32_t slot = x & 0xFFFFu;
-    const uint32_t e0 = T.coarse[(slot >> 8) * kLanes];
-    uint32_t s = (e0 + (x & 0xFFu)) >> 8;
-    uint32_t e = T.tab[s * kLanes];
-    uint32_t r = slot - (e & 0xFFFFu), fm1 = e >> 16;
-    if (__any_sync(kFull, r > fm1)) {  // the slot lies past a second end inside its bucket
-        while (r > fm1 && s < T.hi) {
-            s++;
-            e = T.tab[s * kLanes];
-            r = slot - (e & 0xFFFFu);
-            fm1 = e >> 16;
-        }
-    }
+// State update for the lane's symbol (r = slot - c_s, fm1 = f_s - 1) and
+// the warp's renormalization: lanes whose state fell below 2^16 take the
+// next words of the stream in lane order.
+__device__ __forceinline__ void update(uint32_t &x, uint32_t &pw, const Lut &T, const uint16_t *ring, uint32_t r,
+                                       uint32_t fm1) {
     const uint32_t xh = x >> 16;
     x = xh * fm1 + xh + r;
     const bool need = x < kStateLow;
@@ -260,27 +249,68 @@ __device__ __forceinline__ uint32_t rans_step(uint32_t &x, uint32_t &pw, const L
     const uint32_t w = ring[(pw + __popc(bal & T.lt)) & (kRingWords - 1u)];
     x = need ? __byte_perm(w, x, 0x5410) : x;  // (x << 16) | w
     pw += __popc(bal);
-    return s;
 }
 
+__device__ __forceinline__ uint16_t to_half(float v) { return __half_as_ushort(__float2half_rn(v)); }
+
+// One decode step of the lane's coder: symbol lookup, state update, the
+// warp's renormalization (lanes take the next words in lane order) and the
+// symbol's dequantized delta.  Symbols past a second end inside their bucket
+// and escapes are rare: one vote sends the warp to the path that handles
+// both, and that path walks with a uniform loop so the common path carries
+// no divergence bookkeeping.
 template <bool kHasEsc>
-__device__ __forceinline__ float dequant(uint32_t s, const Lut &T, float step, const int32_t *escapes, uint32_t &ep,
-                                         uint32_t ee) {
-    float dq = T.dq[s];
-    if (kHasEsc) {
-        const uint32_t esb = __ballot_sync(kFull, s == kEsc);
-        if (esb) {
+__device__ __forceinline__ float rans_step(uint32_t &x, uint32_t &pw, const Lut &T, const uint16_t *ring, float step,
+                                           const int32_t *escapes, uint32_t &ep, uint32_t ee) {
+    const uint32_t e0 = T.coarse[((x >> 8) & 0xFFu) * kLanes];
+    uint32_t s = (e0 + (x & 0xFFu)) >> 8;
+    uint32_t e = T.tab[s * kLanes];
+    uint32_t r = (x - e) & 0xFFFFu;  // slot - c_s: the slot never lies before c_s
+    uint32_t fm1 = e >> 16;
+    bool wk = r > fm1;
+    float dq;
+    if (__any_sync(kFull, kHasEsc ? (wk || s == kEsc) : wk)) {
+        while (__any_sync(kFull, wk)) {
+            if (wk) {
+                s++;
+                e = T.tab[s * kLanes];
+                r = (x - e) & 0xFFFFu;
+                fm1 = e >> 16;
+                wk = r > fm1 && s < T.hi;
+            }
+        }
+        dq = T.dq[s];
+        if (kHasEsc) {
+            const uint32_t esb = __ballot_sync(kFull, s == kEsc);
             if (s == kEsc) {
                 const uint32_t idx = ep + __popc(esb & T.lt);
                 dq = __fmul_rn(__int2float_rn(idx < ee ? escapes[idx] : 0), step);
             }
             ep += __popc(esb);
         }
+    } else {
+        dq = T.dq[s];
     }
+    update(x, pw, T, ring, r, fm1);
     return dq;
 }
 
-__device__ __forceinline__ uint16_t to_half(float v) { return __half_as_ushort(__float2half_rn(v)); }
+// Common-path step: exact unless a lane of the warp holds a slot past a
+// second end inside its bucket or an escape.  Then it returns false with
+// nothing changed and the caller repeats the step with rans_step; keeping
+// that path out of the unrolled run leaves the run free of branches.
+template <bool kHasEsc>
+__device__ __forceinline__ bool fast_step(uint32_t &x, uint32_t &pw, const Lut &T, const uint16_t *ring, float xa,
+                                          uint16_t *dst) {
+    const uint32_t e0 = T.coarse[((x >> 8) & 0xFFu) * kLanes];
+    const uint32_t s = (e0 + (x & 0xFFu)) >> 8;
+    const uint32_t e = T.tab[s * kLanes];
+    const uint32_t r = (x - e) & 0xFFFFu, fm1 = e >> 16;
+    if (__any_sync(kFull, kHasEsc ? (r > fm1 || s == kEsc) : r > fm1)) return false;
+    update(x, pw, T, ring, r, fm1);
+    *dst = to_half(__fadd_rn(xa, T.dq[s]));
+    return true;
+}
 
 // Decode stream (slice, grp, span sp) of object o into dst (slice base).
 // kG = 10 / kC = 1024 select compile-time group size / row stride (0: runtime).
@@ -331,8 +361,7 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
         const uint32_t cnt = min(G - gp0, p1 - p);
         for (uint32_t k = 0; k < cnt && K.alive; k++) {
             if (k % kMaxRun == 0) ensure(R, K, pw + kLanes * min(kMaxRun, cnt - k));
-            const uint32_t s = rans_step(x, pw, T, ring);
-            out[(size_t)k * C] = to_half(__fadd_rn(xa, dequant<kHasEsc>(s, T, step, o.escapes, ep, ee)));
+            out[(size_t)k * C] = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
         }
         p += cnt;
         out += (size_t)cnt * C;
@@ -345,16 +374,18 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
         if (p + G < p1) qa_next = arow[C];  // prefetch the next group's anchor
         out[0] = to_half(xa);
         if (kG) ensure(R, K, pw + kLanes * (kG - 1u));  // kG - 1 <= kMaxRun
+        if (kG) {
+            uint32_t k = 1;
 #pragma unroll
-        for (uint32_t k = 1; k < (kG ? kG : 1u); k++) {
-            const uint32_t s = rans_step(x, pw, T, ring);
-            out[(size_t)k * C] = to_half(__fadd_rn(xa, dequant<kHasEsc>(s, T, step, o.escapes, ep, ee)));
-        }
-        if (!kG) {
+            for (; k < (kG ? kG : 1u); k++)
+                if (!fast_step<kHasEsc>(x, pw, T, ring, xa, out + (size_t)k * C)) break;
+#pragma unroll 1
+            for (; k < (kG ? kG : 1u); k++)
+                out[(size_t)k * C] = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
+        } else {
             for (uint32_t k = 1; k < G; k++) {
                 if ((k - 1u) % kMaxRun == 0) ensure(R, K, pw + kLanes * min(kMaxRun, G - k));
-                const uint32_t s = rans_step(x, pw, T, ring);
-                out[(size_t)k * C] = to_half(__fadd_rn(xa, dequant<kHasEsc>(s, T, step, o.escapes, ep, ee)));
+                out[(size_t)k * C] = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
             }
         }
         p += G;
@@ -367,8 +398,7 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
         const uint32_t cnt = p1 - p - 1u;
         for (uint32_t k = 1; k <= cnt && K.alive; k++) {
             if ((k - 1u) % kMaxRun == 0) ensure(R, K, pw + kLanes * min(kMaxRun, cnt - k + 1u));
-            const uint32_t s = rans_step(x, pw, T, ring);
-            out[(size_t)k * C] = to_half(__fadd_rn(xa, dequant<kHasEsc>(s, T, step, o.escapes, ep, ee)));
+            out[(size_t)k * C] = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
         }
     }
     // drain copies still in flight before the ring is reused
