@@ -63,6 +63,10 @@ struct RefDst {
 };
 
 constexpr int kMaxDecWarps = 16;
+// Registers per thread of the decode kernels: 56 x 32 lanes is a whole
+// number of 256-register allocation units, so that three blocks of up to 12
+// warps fit one SM.
+constexpr int kDecRegs = 56;
 constexpr uint32_t kSegBytes = 256;                     // one bulk copy
 constexpr uint32_t kSegWords = kSegBytes / 2;           // 128 words
 constexpr uint32_t kRingSegs = 8;
@@ -464,7 +468,7 @@ __device__ __forceinline__ Ring make_ring(uint8_t *smem, uint32_t nwarps) {
     return R;
 }
 
-__global__ void __launch_bounds__(kMaxDecWarps * 32) k_decode_all(DecObj o, StepTable st, uint16_t *out,
+__global__ void __maxnreg__(kDecRegs) k_decode_all(DecObj o, StepTable st, uint16_t *out,
                                                                       uint32_t *status) {
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t grp = blockIdx.x, slice = blockIdx.y, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -478,7 +482,7 @@ __global__ void __launch_bounds__(kMaxDecWarps * 32) k_decode_all(DecObj o, Step
         if (!decode_span(o, slice, grp, (uint32_t)sp, step, smem, R, dst, 0, status)) break;
 }
 
-__global__ void __launch_bounds__(kMaxDecWarps * 32) k_decode_jobs(const DecObj *objs, const DecJob *jobs,
+__global__ void __maxnreg__(kDecRegs) k_decode_jobs(const DecObj *objs, const DecJob *jobs,
                                                                        const SpanRef *spans, const RefDst *refs,
                                                                        uint32_t *status) {
     extern __shared__ __align__(128) uint8_t smem[];

@@ -88,6 +88,29 @@ def test_escapes_and_extreme_values():
 
 
 @needs_gpu
+def test_equal_spans_escapes_and_unaligned_output():
+    """Five spans of equal length (a multiple of the group size) and a short
+    one, escapes inside them, and an output that is only 2-byte aligned."""
+    L, T, Cc = 2, 530, 96
+    x = synth.ar1_kv(L, T, Cc, 0.9, 2, seed=31)
+    x[0, 0, 5, 3] = 60000.0
+    x[0, 1, 333, 70] = -60000.0
+    x[1, 0, 201:204, 17] = 3000.0
+    pc, enc, oenc = _roundtrip_check(L, T, Cc, 10, 0, 100, x)  # spans 100 x5 + 30
+    assert enc.sizes["n_escapes"] > 0
+    _roundtrip_check(L, T, Cc, 10, 0, 100, synth.ar1_kv(L, T, Cc, 0.9, 2, seed=32), step=[2.0 ** -9, 0.01])
+    odec = O.decode(P.configs(L, T, Cc, 10, 0, 100)[1], oenc)
+    flat = torch.empty(L * 2 * T * Cc + 1, dtype=torch.float16, device="cuda")
+    out = flat[1:].view(L, 2, T, Cc)
+    assert out.data_ptr() % 4 == 2
+    status = C.new_status()
+    C.cg_decode(pc, enc, out, status)
+    torch.cuda.synchronize()
+    assert C.read_status(status) == C.CG_OK
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), odec)
+
+
+@needs_gpu
 def test_huge_step_and_constant_cache():
     L, T, Cc = 2, 200, 64
     _roundtrip_check(L, T, Cc, 10, 0, 64, synth.ar1_kv(L, T, Cc, 0.9, 1, seed=13), step=[1e6, 1e6])
