@@ -367,20 +367,16 @@ __global__ void __launch_bounds__(1024) k_scan(const uint32_t *in, uint64_t n, O
 }
 
 constexpr int kMaxEncWarps = 12;
+constexpr uint32_t kEtabWords = 256 * kLanes;                   // one [symbol][lane] table
+constexpr uint32_t kEncSmemBytes = 2u * kEtabWords * 4u;         // coder table + reciprocals
 
-// floor(x / f) and x mod f for 1 <= f <= 65536 and x < f * 2^16 (so the
-// quotient is < 2^16): a float estimate from the approximate reciprocal is
-// within one of the quotient (relative error < 2^-21), then one integer
-// correction in each direction makes it exact.
-__device__ __forceinline__ void udiv_small(uint32_t x, uint32_t f, uint32_t &q, uint32_t &r) {
-    float rf;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rf) : "f"(__uint2float_rn(f)));
-    q = __float2uint_rz(__fmul_rz(__uint2float_rz(x), rf));
+// floor(x / f) and x mod f for 1 <= f <= 65536 and x < f * 2^16, with
+// m = floor((2^32 - 1) / f) precomputed per symbol: x * m / 2^32 lies in
+// (x/f - 1, x/f], so its integer part is the quotient or one less, and one
+// correction makes it exact.
+__device__ __forceinline__ void udiv_magic(uint32_t x, uint32_t f, uint32_t m, uint32_t &q, uint32_t &r) {
+    q = __umulhi(x, m);
     r = x - q * f;
-    if ((int32_t)r < 0) {
-        q -= 1u;
-        r += f;
-    }
     if (r >= f) {
         q += 1u;
         r -= f;
@@ -397,6 +393,7 @@ struct EncStream {
 // One coder step of the lane's symbol, in reverse order: emit the low half
 // of the state if coding the symbol would overflow it (the warp's emitters
 // write in lane order), then x = floor(x / f) * 2^16 + x mod f + c.
+// etab: [symbol][lane] c | (f - 1) << 16, followed by [symbol][lane] floor((2^32 - 1) / f).
 __device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab, float v, float xa, float inv_step,
                                          uint32_t lane, uint32_t lt, EncStream &S) {
     const int q = __float2int_rn(__fmul_rn(__fsub_rn(v, xa), inv_step));
@@ -414,7 +411,7 @@ __device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab,
             S.e_top -= ne;
         }
     }
-    const uint32_t e = etab[s * kLanes + lane];
+    const uint32_t e = etab[s * kLanes + lane], m = etab[kEtabWords + s * kLanes + lane];
     const uint32_t f = (e >> 16) + 1u, cs = e & 0xFFFFu;
     const bool emit = (S.xs >> 16) >= f;
     const uint32_t mb = __ballot_sync(kFull, emit);
@@ -425,7 +422,7 @@ __device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab,
     }
     S.top -= nem;
     uint32_t qd, rd;
-    udiv_small(S.xs, f, qd, rd);
+    udiv_magic(S.xs, f, m, qd, rd);
     S.xs = (qd << 16) + rd + cs;
 }
 
@@ -506,7 +503,7 @@ __global__ void __launch_bounds__(kMaxEncWarps * 32, 3) k_encode(EncArgs a, Step
     const uint16_t *x = a.kv + (uint64_t)slice * g.T * g.C + c;
     const float step = st.v[slice >> 1];
 
-    __shared__ uint32_t etab[256 * kLanes];  // [symbol][lane]: c | (f - 1) << 16
+    extern __shared__ __align__(16) uint32_t etab[];  // see enc_step
     __shared__ float s_scale[kLanes];
 
     if (warp == 0) {
@@ -522,6 +519,7 @@ __global__ void __launch_bounds__(kMaxEncWarps * 32, 3) k_encode(EncArgs a, Step
         for (uint32_t s = lo; s <= hi; s++) {
             uint32_t fm1 = a.ftab[table * 256u + s];
             etab[s * kLanes + lane] = cum | (fm1 << 16);
+            etab[kEtabWords + s * kLanes + lane] = 0xFFFFFFFFu / (fm1 + 1u);
             if (fits) {
                 a.tables[off + 2u + 2u * (s - lo)] = (uint8_t)(fm1 & 255u);
                 a.tables[off + 3u + 2u * (s - lo)] = (uint8_t)(fm1 >> 8);
@@ -650,7 +648,10 @@ extern "C" cg_status cg_encode(const cg_config *cfg, const uint16_t *kv, void *w
     k_scan<uint32_t, false><<<1, 1024, 0, s>>>(a.twidth, g.n_tables, a.table_off, a.tables_cap, a.status);
     k_scan<uint32_t, false><<<1, 1024, 0, s>>>(a.esc_count, g.n_streams, a.esc_off, a.escapes_cap, a.status);
     const uint32_t enc_warps = (uint32_t)(g.spans_total < (uint64_t)kMaxEncWarps ? g.spans_total : kMaxEncWarps);
-    k_encode<<<grid, enc_warps * 32, 0, s>>>(a, st);
+    static const cudaError_t attr =
+        cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEncSmemBytes);
+    CG_CUDA_TRY(attr);
+    k_encode<<<grid, enc_warps * 32, kEncSmemBytes, s>>>(a, st);
     k_scan<uint64_t, true><<<1, 1024, 0, s>>>(a.words_count, g.n_streams, a.stream_off, a.payload_cap, a.status);
     const uint64_t pack_blocks = (g.n_streams * 32u + 255u) / 256u;
     k_pack<<<(unsigned)pack_blocks, 256, 0, s>>>(a);
