@@ -10,9 +10,17 @@ the launching stream).  Inputs (5.4 GB) are larger than L2, so no flush is
 needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py --workload streamed [--steps K] [--warmup W]
 
 --impl reference times the CPU oracle (the plain C implementation the
 parity tests use) on a bounded sample of the same workload.
+
+--workload streamed measures the streamed batched decode instead: 64
+contexts of a Llama-34B-shaped cache (48 layers x {K,V} x 8x128, lengths
+uniform in 1.4K-16K tokens, about 112 GB of fp16), each encoded on the GPU
+and held compressed in pinned host memory as 1536-token chunks; one step
+streams every context through the device (H2D copies of each stage's
+chunk ranges on a copy stream, cg_decode_chunks on a compute stream).
 """
 from __future__ import annotations
 
@@ -173,6 +181,63 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_streamed(args):
+    """--workload streamed: decode pipelined against chunked H2D copies."""
+    from kv_cache_compression_decode_gb300 import codec as C
+    from kv_cache_compression_decode_gb300 import pipeline as PL
+    from kv_cache_compression_decode_gb300 import synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    lens = synth.stream_context_lengths()
+    L, Cc, chunk = synth.STREAM_L, synth.STREAM_C, synth.STREAM_CHUNK
+    tps = args.stream_tps
+    ctx, comp = [], 0
+    for j, T in enumerate(lens):
+        x = synth.stream_context(j, T, device=dev)
+        cfg = C.Config(L, T, Cc, 10, chunk, tps, C.layer_steps(L))
+        enc = C.encode(cfg, x)
+        comp += enc.sizes["total_bytes"]
+        ctx.append(PL.HostObject.from_device(cfg, enc))
+        del x, enc
+    torch.cuda.synchronize(dev)
+    sd = PL.StreamedDecoder(ctx, dev, slots=args.stream_slots, chunks_per_stage=args.stream_cps)
+    for _ in range(max(3, args.warmup)):
+        sd.run(timing=False)
+    # the pipeline's last context against a direct decode of the same object
+    last = ctx[-1]
+    direct = C.decode(last.cfg, last.enc.to(dev))
+    check = bool(torch.equal(direct, sd.out_view(len(ctx) - 1)))
+    del direct
+    runs = []
+    with Clocks(dev.index) as clk:
+        for _ in range(args.steps):
+            runs.append(sd.run(timing=True))
+    fp16 = runs[0]["fp16_bytes"]
+    ms = statistics.median(r["total_ms"] for r in runs)
+    pick = lambda k: round(statistics.median(r[k] for r in runs), 4)
+    line = {
+        "metric": "streamed decode: fp16 KV GB/s with compressed chunks streamed from pinned host memory",
+        "value": round(fp16 / (ms * 1e-3) / 1e9, 2), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32+u32", "data": "synthetic",
+        "config": {"workload": f"llama34b-48L-8x128-{len(lens)}ctx-streamed", "contexts": len(lens),
+                   "tokens": int(sum(lens)), "fp16_bytes": fp16, "compressed_bytes": comp,
+                   "bits_per_value": round(8 * comp / (fp16 / 2), 4), "chunk_tokens": chunk,
+                   "tokens_per_stream": tps, "chunks_per_stage": args.stream_cps, "slots": args.stream_slots,
+                   "step": "every context: H2D of its chunks (copy stream) overlapped with cg_decode_chunks "
+                           "(compute stream)"},
+        "h2d_gbs": pick("h2d_gbs"), "h2d_bytes_per_step": runs[0]["h2d_bytes"], "h2d_ms": pick("h2d_ms"),
+        "decode_ms": pick("decode_ms"), "overlap_efficiency": pick("overlap_efficiency"),
+        "decode_gbs_fp16": round(fp16 / (pick("decode_ms") * 1e-3) / 1e9, 2),
+        "last_context_equals_direct_decode": check, "gpu_launches": len(sd.stages) * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if not check:
+        raise SystemExit("streamed decode differs from the direct decode")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -181,11 +246,18 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default="llama70b", choices=["llama70b", "streamed"])
+    ap.add_argument("--stream-tps", type=int, default=768, help="streamed: tokens per stream")
+    ap.add_argument("--stream-cps", type=int, default=6, help="streamed: chunks per pipeline stage")
+    ap.add_argument("--stream-slots", type=int, default=3, help="streamed: staging slots")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: use the first N layers of the workload (not a bench line)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.workload == "streamed":
+        run_streamed(args)
         return
 
     from kv_cache_compression_decode_gb300 import codec as C

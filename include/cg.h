@@ -257,6 +257,45 @@ cg_status cg_deserialize_header(const void *buf, size_t len, cg_config *cfg, flo
  * capacities at least the sizes from cg_deserialize_header). */
 cg_status cg_deserialize(const void *buf, size_t len, const cg_encoded *obj);
 
+/*
+ * Bandwidth-adaptive quality level per chunk (host only).
+ * ("CacheGen vs 传统量化KV缓存压缩技术深度对比与性能测试", §2.2: every chunk is
+ * stored at several quality levels, and the sender picks a level chunk by
+ * chunk from the bandwidth it sees, so that transfer plus decode meets the
+ * service-level deadline.)
+ *
+ * Chunks go out in order over one link and are decoded in order on the GPU;
+ * the decode of a chunk overlaps the transfer of the next.  For chunk i the
+ * planner predicts the bandwidth as the throughput the link gave chunk i - 1
+ * (the trace's first entry for chunk 0).  It takes the highest quality (the
+ * lowest level index) whose predicted completion of the whole context --
+ * chunk i at that level and every later chunk at the lowest quality, at the
+ * predicted bandwidth -- is within slo_s; when no level fits it takes the
+ * lowest quality.  The chunk's transfer is then played against the trace
+ * (piecewise constant, slot_s seconds per entry, the last entry holding on).
+ */
+typedef struct {
+    uint32_t n_chunks, n_levels; /* levels: 0 = highest quality */
+    const uint64_t *bytes;       /* host [n_chunks][n_levels]: bytes sent for chunk c at level q */
+    const double *decode_s;      /* host [n_chunks][n_levels]: GPU decode seconds of chunk c at level q */
+    const double *bw;            /* host [n_slots]: link bandwidth in bytes per second, > 0 */
+    uint32_t n_slots;
+    double slot_s;               /* seconds per trace entry, > 0 */
+    double slo_s;                /* deadline, seconds from the first byte sent */
+} cg_level_plan;
+
+typedef struct {
+    double arrive_s; /* last byte of the chunk received */
+    double done_s;   /* decode of the chunk finished */
+} cg_chunk_time;
+
+/* Fills level[n_chunks] and time[n_chunks] (host, caller-owned) with the plan
+ * and its timeline under the trace, and *finish_s with the time the last
+ * chunk is decoded.  CG_ERR_INVALID_ARG for null pointers, zero counts, or
+ * sizes, times and bandwidths that are negative, non-finite or (bandwidth,
+ * slot length) zero. */
+cg_status cg_plan_levels(const cg_level_plan *p, uint32_t *level, cg_chunk_time *time, double *finish_s);
+
 #ifdef __cplusplus
 }
 #endif

@@ -72,11 +72,21 @@ class cg_chunk_range(ct.Structure):
         "anchor_begin", "anchor_end")]
 
 
+class cg_level_plan(ct.Structure):
+    _fields_ = [("n_chunks", ct.c_uint32), ("n_levels", ct.c_uint32), ("bytes", ct.c_void_p),
+                ("decode_s", ct.c_void_p), ("bw", ct.c_void_p), ("n_slots", ct.c_uint32), ("slot_s", ct.c_double),
+                ("slo_s", ct.c_double)]
+
+
+class cg_chunk_time(ct.Structure):
+    _fields_ = [("arrive_s", ct.c_double), ("done_s", ct.c_double)]
+
+
 # Every symbol libcg exports (the declarations of include/cg.h).
 EXPORTS = ("cg_status_string", "cg_status_from_flags", "cg_encode_bounds", "cg_encode", "cg_decode",
            "cg_decode_chunks_ws_bytes", "cg_decode_chunks", "cg_decode_chunks_noalloc", "cg_chunk_ranges",
            "cg_serialize",
-           "cg_deserialize_header", "cg_deserialize")
+           "cg_deserialize_header", "cg_deserialize", "cg_plan_levels")
 
 _lib = None
 
@@ -102,6 +112,7 @@ def lib() -> ct.CDLL:
                                    ct.POINTER(ct.c_size_t)]
         L.cg_deserialize_header.argtypes = [P, ct.c_size_t, ct.POINTER(cg_config), P, ct.POINTER(cg_sizes)]
         L.cg_deserialize.argtypes = [P, ct.c_size_t, ct.POINTER(cg_encoded)]
+        L.cg_plan_levels.argtypes = [ct.POINTER(cg_level_plan), P, P, ct.POINTER(ct.c_double)]
         for name in EXPORTS:
             if name not in ("cg_status_string",):
                 getattr(L, name).restype = ct.c_int
@@ -320,6 +331,32 @@ def cg_chunk_ranges(cfg: Config, chunk: int, stream_off: np.ndarray, esc_off: np
     _check(lib().cg_chunk_ranges(ct.byref(cfg.c()), chunk, so.ctypes.data, eo.ctypes.data, ct.byref(r)),
            "cg_chunk_ranges")
     return {n: int(getattr(r, n)) for n, _ in r._fields_}
+
+
+@dataclasses.dataclass
+class LevelPlan:
+    levels: np.ndarray   # [n_chunks] chosen level (0 = highest quality)
+    arrive_s: np.ndarray  # [n_chunks] last byte received
+    done_s: np.ndarray    # [n_chunks] decode finished
+    finish_s: float
+
+
+def cg_plan_levels(bytes_: np.ndarray, decode_s: np.ndarray, bw: np.ndarray, slot_s: float,
+                   slo_s: float) -> LevelPlan:
+    """Quality level per chunk for a bandwidth trace and a deadline.
+    bytes_ / decode_s: [n_chunks][n_levels]; bw: bytes/s per trace slot."""
+    b = np.ascontiguousarray(bytes_, dtype=np.uint64)
+    d = np.ascontiguousarray(decode_s, dtype=np.float64)
+    w = np.ascontiguousarray(bw, dtype=np.float64)
+    assert b.ndim == 2 and d.shape == b.shape and w.ndim == 1
+    n, q = b.shape
+    p = cg_level_plan(n, q, b.ctypes.data, d.ctypes.data, w.ctypes.data, len(w), float(slot_s), float(slo_s))
+    lv = np.zeros(n, dtype=np.uint32)
+    tm = (cg_chunk_time * max(n, 1))()
+    fin = ct.c_double()
+    _check(lib().cg_plan_levels(ct.byref(p), lv.ctypes.data, ct.addressof(tm), ct.byref(fin)), "cg_plan_levels")
+    return LevelPlan(lv, np.array([t.arrive_s for t in tm[:n]]), np.array([t.done_s for t in tm[:n]]),
+                     float(fin.value))
 
 
 def cg_serialize(cfg: Config, host: Encoded) -> bytes:

@@ -5,6 +5,7 @@
 // quality level) before streaming it ("CacheGen vs 传统量化KV缓存压缩技术深度
 // 对比与性能测试", §2.2): header + sections, each section starting on a
 // 16-byte boundary so the payload can be used in place.
+#include <math.h>
 #include <string.h>
 
 #include "cg_internal.cuh"
@@ -186,5 +187,73 @@ extern "C" cg_status cg_deserialize(const void *buf, size_t len, const cg_encode
         if (parts[i]) memcpy(dst[i], p, parts[i]);
         p += round_up(parts[i], 16);
     }
+    return CG_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Level planner ("CacheGen vs 传统量化KV缓存压缩技术深度对比与性能测试", §2.2).
+// ---------------------------------------------------------------------------
+namespace {
+
+// End of a transfer of `bytes` that starts at t0 under the piecewise-constant
+// trace (slot k covers [k slot_s, (k + 1) slot_s); the last slot holds on).
+double transfer_end(const cg_level_plan &p, double t0, double bytes) {
+    double t = t0, rem = bytes;
+    double kf = floor(t / p.slot_s);
+    uint32_t k = kf >= (double)(p.n_slots - 1) ? p.n_slots - 1 : (uint32_t)kf;
+    for (; k + 1 < p.n_slots; k++) {
+        const double end = (double)(k + 1) * p.slot_s;
+        if (end <= t) continue;
+        const double cap = (end - t) * p.bw[k];
+        if (cap >= rem) return t + rem / p.bw[k];
+        rem -= cap;
+        t = end;
+    }
+    return t + rem / p.bw[p.n_slots - 1];
+}
+
+// Completion of the context if chunk i takes level q and every later chunk
+// the lowest quality, at constant bandwidth b, from link/GPU free times.
+double predict_finish(const cg_level_plan &p, uint32_t i, uint32_t q, double t_link, double t_gpu, double b) {
+    const uint32_t Q = p.n_levels, low = Q - 1;
+    double tl = t_link + (double)p.bytes[(uint64_t)i * Q + q] / b;
+    double tg = fmax(tl, t_gpu) + p.decode_s[(uint64_t)i * Q + q];
+    for (uint32_t j = i + 1; j < p.n_chunks; j++) {
+        tl += (double)p.bytes[(uint64_t)j * Q + low] / b;
+        tg = fmax(tl, tg) + p.decode_s[(uint64_t)j * Q + low];
+    }
+    return tg;
+}
+
+bool finite_nonneg(double v) { return isfinite(v) && v >= 0.0; }
+
+}  // namespace
+
+extern "C" cg_status cg_plan_levels(const cg_level_plan *p, uint32_t *level, cg_chunk_time *time, double *finish_s) {
+    if (!p || !level || !time || !finish_s || !p->bytes || !p->decode_s || !p->bw) return CG_ERR_INVALID_ARG;
+    if (p->n_chunks == 0 || p->n_levels == 0 || p->n_slots == 0) return CG_ERR_INVALID_ARG;
+    if (!(isfinite(p->slot_s) && p->slot_s > 0.0) || !finite_nonneg(p->slo_s)) return CG_ERR_INVALID_ARG;
+    for (uint32_t k = 0; k < p->n_slots; k++)
+        if (!(isfinite(p->bw[k]) && p->bw[k] > 0.0)) return CG_ERR_INVALID_ARG;
+    for (uint64_t k = 0; k < (uint64_t)p->n_chunks * p->n_levels; k++)
+        if (!finite_nonneg(p->decode_s[k])) return CG_ERR_INVALID_ARG;
+    double t_link = 0.0, t_gpu = 0.0, b = p->bw[0];
+    for (uint32_t i = 0; i < p->n_chunks; i++) {
+        uint32_t q = p->n_levels - 1;
+        for (uint32_t c = 0; c + 1 < p->n_levels; c++)
+            if (predict_finish(*p, i, c, t_link, t_gpu, b) <= p->slo_s) {
+                q = c;
+                break;
+            }
+        const double bytes = (double)p->bytes[(uint64_t)i * p->n_levels + q];
+        const double arrive = transfer_end(*p, t_link, bytes);
+        if (arrive > t_link) b = bytes / (arrive - t_link);  // throughput seen by this chunk
+        t_gpu = fmax(arrive, t_gpu) + p->decode_s[(uint64_t)i * p->n_levels + q];
+        t_link = arrive;
+        level[i] = q;
+        time[i].arrive_s = arrive;
+        time[i].done_s = t_gpu;
+    }
+    *finish_s = t_gpu;
     return CG_OK;
 }

@@ -60,15 +60,33 @@ def _span(ranges: Sequence[dict], key: str):
 
 class StreamedDecoder:
     """Decodes a sequence of compressed contexts, `chunks_per_stage` chunks
-    at a time, with H2D copies on one stream and decode on another."""
+    at a time, with H2D copies on one stream and decode on another.
 
-    def __init__(self, contexts: Sequence[HostObject], device="cuda", slots: int = 3, chunks_per_stage: int = 1,
+    A context is one HostObject, or -- with `levels` -- one HostObject per
+    quality level (the same cache encoded with different steps) together
+    with the level of each of its chunks (levels[j][c]), as chosen for
+    instance by codec.cg_plan_levels; every chunk is then copied from, and
+    decoded with the tables of, its own level."""
+
+    def __init__(self, contexts: Sequence, device="cuda", slots: int = 3, chunks_per_stage: int = 1,
                  copy_fn: Optional[Callable[[torch.Tensor, torch.Tensor], None]] = None,
-                 outputs: Optional[Sequence[torch.Tensor]] = None):
+                 outputs: Optional[Sequence[torch.Tensor]] = None,
+                 levels: Optional[Sequence[Sequence[int]]] = None):
         """outputs: optional device fp16 tensor [L][2][T][C] per context;
         without it two buffers alternate between contexts (the decoded
         context is overwritten two contexts later)."""
-        self.ctx = list(contexts)
+        if levels is None:
+            self.objs = [[h] for h in contexts]
+            self.lv = [[0] * h.n_chunks for h in contexts]
+        else:
+            self.objs = [list(h) for h in contexts]
+            self.lv = [list(map(int, l)) for l in levels]
+            for j, (os_, lv) in enumerate(zip(self.objs, self.lv)):
+                g = [(o.cfg.L, o.cfg.T, o.cfg.C, o.cfg.group_size, o.cfg.chunk_tokens, o.cfg.tokens_per_stream)
+                     for o in os_]
+                if len(set(g)) != 1 or len(lv) != os_[0].n_chunks or not all(0 <= q < len(os_) for q in lv):
+                    raise ValueError(f"context {j}: levels do not match its objects")
+        self.ctx = [os_[0] for os_ in self.objs]  # geometry of each context
         self.outputs = list(outputs) if outputs is not None else None
         self.dev = torch.device(device)
         self.N = slots
@@ -81,21 +99,20 @@ class StreamedDecoder:
                 self.stages.append((j, c0, min(c0 + self.cps, h.n_chunks)))
         mx = {"payload": 16, "escape": 1, "anchor": 1}
         for j, c0, c1 in self.stages:
-            r = self.ctx[j].ranges[c0:c1]
             for k in mx:
-                b, e = _span(r, k)
-                mx[k] = max(mx[k], e - b)
+                mx[k] = max(mx[k], sum(self._len(j, c, k) for c in range(c0, c1)))
         u8, i32 = torch.uint8, torch.int32
         self.slot_payload = [torch.empty(mx["payload"], dtype=u8, device=self.dev) for _ in range(self.N)]
         self.slot_esc = [torch.empty(mx["escape"], dtype=i32, device=self.dev) for _ in range(self.N)]
         self.slot_anc = [torch.empty(mx["anchor"], dtype=torch.int8, device=self.dev) for _ in range(self.N)]
-        # two device headers and two output buffers, alternating by context
+        # two sets of device headers (one per level) and two output buffers, alternating by context
         hdr_fields = ["scales", "tables", "table_off", "stream_off", "esc_off"]
         self.hdr_fields = hdr_fields
-        mxh = {f: max(getattr(h.enc, f).numel() for h in self.ctx) for f in hdr_fields}
+        nlev = max(len(os_) for os_ in self.objs)
+        mxh = {f: max(getattr(o.enc, f).numel() for os_ in self.objs for o in os_) for f in hdr_fields}
         dts = {f: getattr(self.ctx[0].enc, f).dtype for f in hdr_fields}
-        self.hdr = [{f: torch.empty(max(mxh[f], 1), dtype=dts[f], device=self.dev) for f in hdr_fields}
-                    for _ in range(2)]
+        self.hdr = [[{f: torch.empty(max(mxh[f], 1), dtype=dts[f], device=self.dev) for f in hdr_fields}
+                     for _ in range(nlev)] for _ in range(2)]
         mxo = max(h.cfg.L * 2 * h.cfg.T * h.cfg.C for h in self.ctx) if outputs is None else 1
         self.out_buf = [torch.empty(mxo, dtype=torch.float16, device=self.dev) for _ in range(2)]
         self.copy_stream = torch.cuda.Stream(self.dev)
@@ -104,10 +121,24 @@ class StreamedDecoder:
         # descriptor workspace per slot
         ws = 256
         for j, c0, c1 in self.stages:
-            ws = max(ws, C.cg_decode_chunks_ws_bytes(self._refs(j, c0, c1, self.slot_payload[0], self.slot_esc[0],
-                                                                   self.slot_anc[0], self.hdr[0])))
+            ws = max(ws, C.cg_decode_chunks_ws_bytes(self._refs(j, c0, c1, 0, self._place(j, c0, c1))))
         self.ws = [torch.empty(ws, dtype=torch.uint8, device=self.dev) for _ in range(self.N)]
         self.stats = {}
+
+    def _len(self, j: int, c: int, key: str) -> int:
+        r = self.objs[j][self.lv[j][c]].ranges[c]
+        return r[key + "_end"] - r[key + "_begin"]
+
+    def _place(self, j: int, c0: int, c1: int):
+        """Offsets of each chunk's payload / escape / anchor ranges in a slot.
+        Consecutive chunks of one level are one contiguous range (chunk-major
+        sections), so they are copied together."""
+        place, off = [], {"payload": 0, "escape": 0, "anchor": 0}
+        for c in range(c0, c1):
+            place.append(dict(off))
+            for k in off:
+                off[k] += self._len(j, c, k)
+        return place
 
     def out_view(self, j: int) -> torch.Tensor:
         if self.outputs is not None:
@@ -115,20 +146,32 @@ class StreamedDecoder:
         cfg = self.ctx[j].cfg
         return self.out_buf[j % 2][: cfg.L * 2 * cfg.T * cfg.C].view(cfg.L, 2, cfg.T, cfg.C)
 
-    def _refs(self, j, c0, c1, sp, se, sa, hdr):
-        h = self.ctx[j]
-        r = h.ranges[c0:c1]
-        pb, pe = _span(r, "payload")
-        eb, ee = _span(r, "escape")
-        ab, ae = _span(r, "anchor")
-        raw = C.RawEncoded(anchors=sa.data_ptr() - ab, scales=hdr["scales"].data_ptr(),
-                           tables=hdr["tables"].data_ptr(), table_off=hdr["table_off"].data_ptr(),
-                           payload=sp.data_ptr() - pb, stream_off=hdr["stream_off"].data_ptr(),
-                           escapes=se.data_ptr() - 4 * eb, esc_off=hdr["esc_off"].data_ptr(),
-                           tables_cap=h.enc.tables.numel(), payload_cap=pe, escapes_cap=ee)
-        cfg = h.cfg
+    def _refs(self, j, c0, c1, slot, place):
+        """Chunk refs of a stage.  A run of consecutive chunks at one level
+        lies contiguously in the slot and in its object's sections, so the
+        run shares one view of the object (and one set of decode blocks)."""
+        sp, se, sa = self.slot_payload[slot], self.slot_esc[slot], self.slot_anc[slot]
         dst = self.out_view(j)
-        return [C.ChunkRef(cfg, raw, ch, dst, ch * cfg.chunk_tokens) for ch in range(c0, c1)]
+        refs = []
+        c = c0
+        while c < c1:
+            q = self.lv[j][c]
+            e = c
+            while e + 1 < c1 and self.lv[j][e + 1] == q:
+                e += 1
+            h, hdr, pl = self.objs[j][q], self.hdr[j % 2][q], place[c - c0]
+            rb, re_ = h.ranges[c], h.ranges[e]
+            raw = C.RawEncoded(anchors=sa.data_ptr() + pl["anchor"] - rb["anchor_begin"],
+                               scales=hdr["scales"].data_ptr(), tables=hdr["tables"].data_ptr(),
+                               table_off=hdr["table_off"].data_ptr(),
+                               payload=sp.data_ptr() + pl["payload"] - rb["payload_begin"],
+                               stream_off=hdr["stream_off"].data_ptr(),
+                               escapes=se.data_ptr() + 4 * (pl["escape"] - rb["escape_begin"]),
+                               esc_off=hdr["esc_off"].data_ptr(), tables_cap=h.enc.tables.numel(),
+                               payload_cap=re_["payload_end"], escapes_cap=re_["escape_end"])
+            refs += [C.ChunkRef(h.cfg, raw, k, dst, k * h.cfg.chunk_tokens) for k in range(c, e + 1)]
+            c = e + 1
+        return refs
 
     def run(self, timing: bool = True) -> dict:
         """Stream every stage through the pipeline; returns timing stats."""
@@ -147,30 +190,40 @@ class StreamedDecoder:
         h2d_bytes = 0
         error = None
         for i, (j, c0, c1) in enumerate(self.stages):
-            h = self.ctx[j]
             slot = i % N
+            place = self._place(j, c0, c1)
             try:
                 with torch.cuda.stream(self.copy_stream):
                     if i >= N:
                         self.copy_stream.wait_event(free[i - N])
                     if timing:
                         copy_ev[i][0].record(self.copy_stream)
-                    if c0 == 0:  # context header into header slot j % 2
+                    if c0 == 0:  # the context's headers (one per level used) into header set j % 2
                         if j >= 2:
                             self.copy_stream.wait_event(hdr_free[j - 2])
-                        for f in self.hdr_fields:
-                            src = getattr(h.enc, f)
-                            if src.numel():
-                                self.copy_fn(self.hdr[j % 2][f][: src.numel()], src)
-                                h2d_bytes += src.numel() * src.element_size()
-                    r = h.ranges[c0:c1]
-                    for key, dst, src, scale in (("payload", self.slot_payload[slot], h.enc.payload, 1),
-                                                 ("escape", self.slot_esc[slot], h.enc.escapes, 1),
-                                                 ("anchor", self.slot_anc[slot], h.enc.anchors, 1)):
-                        b, e = _span(r, key)
-                        if e > b:
-                            self.copy_fn(dst[: e - b], src[b:e])
-                            h2d_bytes += (e - b) * src.element_size()
+                        for q in sorted(set(self.lv[j])):
+                            for f in self.hdr_fields:
+                                src = getattr(self.objs[j][q].enc, f)
+                                if src.numel():
+                                    self.copy_fn(self.hdr[j % 2][q][f][: src.numel()], src)
+                                    h2d_bytes += src.numel() * src.element_size()
+                    # runs of consecutive chunks at one level: one copy per section
+                    c = c0
+                    while c < c1:
+                        q = self.lv[j][c]
+                        e = c
+                        while e + 1 < c1 and self.lv[j][e + 1] == q:
+                            e += 1
+                        h = self.objs[j][q]
+                        for key, dst, src in (("payload", self.slot_payload[slot], h.enc.payload),
+                                              ("escape", self.slot_esc[slot], h.enc.escapes),
+                                              ("anchor", self.slot_anc[slot], h.enc.anchors)):
+                            b, en = h.ranges[c][key + "_begin"], h.ranges[e][key + "_end"]
+                            o = place[c - c0][key]
+                            if en > b:
+                                self.copy_fn(dst[o: o + en - b], src[b:en])
+                                h2d_bytes += (en - b) * src.element_size()
+                        c = e + 1
                     if timing:
                         copy_ev[i][1].record(self.copy_stream)
                     ready[i].record(self.copy_stream)
@@ -181,13 +234,12 @@ class StreamedDecoder:
                 self.compute_stream.wait_event(ready[i])
                 if timing:
                     dec_ev[i][0].record(self.compute_stream)
-                refs = self._refs(j, c0, c1, self.slot_payload[slot], self.slot_esc[slot], self.slot_anc[slot],
-                                  self.hdr[j % 2])
+                refs = self._refs(j, c0, c1, slot, place)
                 C.cg_decode_chunks(refs, self.ws[slot], self.status, self.compute_stream)
                 if timing:
                     dec_ev[i][1].record(self.compute_stream)
                 free[i].record(self.compute_stream)
-                if c1 == h.n_chunks:
+                if c1 == self.ctx[j].n_chunks:
                     hdr_free[j] = torch.cuda.Event()
                     hdr_free[j].record(self.compute_stream)
         self.copy_stream.wait_stream(self.compute_stream)

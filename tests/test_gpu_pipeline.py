@@ -77,3 +77,42 @@ def test_transfer_failure_is_reported_and_context_survives():
     sd2.run()
     for o, e in zip(outs, expect):
         assert np.array_equal(o.cpu().numpy().view(np.uint16), e)
+
+
+@needs_gpu
+def test_planned_levels_drive_the_stream():
+    """cg_plan_levels picks a quality level per chunk for a deadline between
+    the all-lowest and the all-highest transfer times; the streamed decode
+    then fetches every chunk from, and decodes it with, its level's object."""
+    L, Cc, chunk, tps = 2, 64, 128, 128
+    objs_all, odecs_all, levels = [], [], []
+    for j, T in enumerate([700, 450]):
+        x = synth.ar1_kv(L, T, Cc, 0.95, 1, seed=40 + j)
+        objs, odecs = [], []
+        for m in synth.LEVEL_MULTIPLIERS:
+            pc, oc = P.configs(L, T, Cc, 10, chunk, tps, m)
+            objs.append(PL.HostObject.from_device(pc, C.encode(pc, x.cuda())))
+            odecs.append(O.decode(oc, O.encode(oc, x.numpy().view(np.uint16))))
+        n = objs[0].n_chunks
+        size = lambda h, c: sum((h.ranges[c][k + "_end"] - h.ranges[c][k + "_begin"]) * w
+                                for k, w in (("payload", 1), ("anchor", 1), ("escape", 4)))
+        nbytes = np.array([[size(h, c) for h in objs] for c in range(n)], dtype=np.uint64)
+        dec = np.full(nbytes.shape, 1e-6)
+        bw = np.array([1e6])
+        hi = C.cg_plan_levels(nbytes, dec, bw, 1.0, 1e9).finish_s
+        lo = C.cg_plan_levels(nbytes, dec, bw, 1.0, 0.0).finish_s
+        plan = C.cg_plan_levels(nbytes, dec, bw, 1.0, 0.5 * (hi + lo))
+        assert plan.finish_s <= 0.5 * (hi + lo)
+        assert len(set(plan.levels.tolist())) > 1, plan.levels
+        objs_all.append(objs)
+        odecs_all.append(odecs)
+        levels.append(plan.levels)
+    outs = [torch.full((L, 2, h[0].cfg.T, Cc), float("nan"), dtype=torch.float16, device="cuda") for h in objs_all]
+    sd = PL.StreamedDecoder(objs_all, "cuda", slots=2, chunks_per_stage=2, outputs=outs, levels=levels)
+    sd.run()
+    for j, (o, lv) in enumerate(zip(outs, levels)):
+        got = o.cpu().numpy().view(np.uint16)
+        T = got.shape[2]
+        for c, q in enumerate(lv):
+            sl = slice(c * chunk, min(T, (c + 1) * chunk))
+            assert np.array_equal(got[:, :, sl], odecs_all[j][q][:, :, sl]), f"context {j} chunk {c} level {q}"
