@@ -228,6 +228,37 @@ cg_status cg_decode_chunks(const cg_chunk_ref *refs, uint32_t n, void *ws, size_
 #define CG_NOALLOC_DESC_BYTES (4u << 20)
 cg_status cg_decode_chunks_noalloc(const cg_chunk_ref *refs, uint32_t n, uint32_t *dev_status, void *stream);
 
+/*
+ * Paged destination: the fp16 cache as fixed-size token blocks scattered in
+ * a pool, as a serving engine keeps it (the decoded cache goes straight into
+ * the engine's blocks; "CacheGen: KV Cache Compression and Streaming for
+ * Fast Large Language Model Serving", gptget.net page, method details: the
+ * decoded KV is handed to the serving LLM).  Element (layer l, K/V kv,
+ * token t, channel c) is
+ *     pool[l * layer_stride + kv * kv_stride + block_table[t / block_tokens] * block_stride
+ *          + (t % block_tokens) * token_stride + c]
+ * (strides in fp16 elements; a token's C channels are contiguous).  For the
+ * per-layer layout [L][n_pool][2][block_tokens][C], for instance:
+ * layer_stride = n_pool * 2 * block_tokens * C, block_stride = 2 * block_tokens
+ * * C, kv_stride = block_tokens * C, token_stride = C.
+ */
+typedef struct {
+    uint16_t *pool;              /* device */
+    const uint32_t *block_table; /* device [n_blocks]: physical block of logical block i */
+    uint32_t n_blocks;           /* logical blocks; n_blocks * block_tokens >= T */
+    uint32_t n_pool_blocks;      /* physical blocks in the pool */
+    uint32_t block_tokens;       /* a power of two, >= group_size */
+    uint64_t layer_stride, kv_stride, block_stride, token_stride;
+} cg_paged_kv;
+
+/* cg_decode into a paged destination: the same decode, every token row
+ * stored through the block table.  A block-table entry >= n_pool_blocks
+ * sets CG_ERR_RANGE in *dev_status and the streams that reach it stop
+ * before writing to it.  Host checks (CG_ERR_INVALID_ARG): null pointers,
+ * block_tokens not a power of two or below group_size, too few blocks. */
+cg_status cg_decode_paged(const cg_config *cfg, const cg_encoded *enc, const cg_paged_kv *dst, uint32_t *dev_status,
+                          void *stream);
+
 /* Where chunk `chunk` lives inside the per-chunk sections: byte ranges of
  * payload and anchors, entry range of escapes, and entry ranges of
  * stream_off / esc_off that describe it.  Host only; `off` arrays are host

@@ -72,6 +72,12 @@ class cg_chunk_range(ct.Structure):
         "anchor_begin", "anchor_end")]
 
 
+class cg_paged_kv(ct.Structure):
+    _fields_ = [("pool", ct.c_void_p), ("block_table", ct.c_void_p), ("n_blocks", ct.c_uint32),
+                ("n_pool_blocks", ct.c_uint32), ("block_tokens", ct.c_uint32), ("layer_stride", ct.c_uint64),
+                ("kv_stride", ct.c_uint64), ("block_stride", ct.c_uint64), ("token_stride", ct.c_uint64)]
+
+
 class cg_level_plan(ct.Structure):
     _fields_ = [("n_chunks", ct.c_uint32), ("n_levels", ct.c_uint32), ("bytes", ct.c_void_p),
                 ("decode_s", ct.c_void_p), ("bw", ct.c_void_p), ("n_slots", ct.c_uint32), ("slot_s", ct.c_double),
@@ -86,7 +92,7 @@ class cg_chunk_time(ct.Structure):
 EXPORTS = ("cg_status_string", "cg_status_from_flags", "cg_encode_bounds", "cg_encode", "cg_decode",
            "cg_decode_chunks_ws_bytes", "cg_decode_chunks", "cg_decode_chunks_noalloc", "cg_chunk_ranges",
            "cg_serialize",
-           "cg_deserialize_header", "cg_deserialize", "cg_plan_levels")
+           "cg_deserialize_header", "cg_deserialize", "cg_plan_levels", "cg_decode_paged")
 
 _lib = None
 
@@ -113,6 +119,7 @@ def lib() -> ct.CDLL:
         L.cg_deserialize_header.argtypes = [P, ct.c_size_t, ct.POINTER(cg_config), P, ct.POINTER(cg_sizes)]
         L.cg_deserialize.argtypes = [P, ct.c_size_t, ct.POINTER(cg_encoded)]
         L.cg_plan_levels.argtypes = [ct.POINTER(cg_level_plan), P, P, ct.POINTER(ct.c_double)]
+        L.cg_decode_paged.argtypes = [ct.POINTER(cg_config), ct.POINTER(cg_encoded), ct.POINTER(cg_paged_kv), P, P]
         for name in EXPORTS:
             if name not in ("cg_status_string",):
                 getattr(L, name).restype = ct.c_int
@@ -272,6 +279,23 @@ def cg_decode(cfg: Config, enc: Encoded, kv_out: torch.Tensor, status: torch.Ten
     code = lib().cg_decode(ct.byref(cfg.c()), ct.byref(enc.c()), kv_out.data_ptr(), status.data_ptr(),
                            _stream_ptr(stream))
     _check(code, "cg_decode")
+
+
+def cg_decode_paged(cfg: Config, enc, pool: torch.Tensor, block_table: torch.Tensor, block_tokens: int,
+                    layer_stride: int, kv_stride: int, block_stride: int, token_stride: int,
+                    status: torch.Tensor, stream=None, n_pool_blocks: Optional[int] = None) -> None:
+    """Enqueue a decode whose token rows go to the blocks of a paged pool
+    (fp16); block_table is a device int32/uint32 tensor of logical -> physical
+    blocks.  Strides are in fp16 elements."""
+    assert pool.dtype == torch.float16 and block_table.dtype in (torch.int32, torch.uint32)
+    assert block_table.is_contiguous()
+    if n_pool_blocks is None:
+        n_pool_blocks = (pool.numel() - 1) // max(block_stride, 1) + 1
+    d = cg_paged_kv(pool.data_ptr(), block_table.data_ptr(), block_table.numel(), n_pool_blocks, block_tokens,
+                    layer_stride, kv_stride, block_stride, token_stride)
+    code = lib().cg_decode_paged(ct.byref(cfg.c()), ct.byref(enc.c()), ct.byref(d), status.data_ptr(),
+                                 _stream_ptr(stream) if pool.is_cuda else None)
+    _check(code, "cg_decode_paged")
 
 
 @dataclasses.dataclass

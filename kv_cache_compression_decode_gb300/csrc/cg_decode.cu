@@ -316,13 +316,69 @@ __device__ __forceinline__ bool fast_step(uint32_t &x, uint32_t &pw, const Lut &
     return true;
 }
 
-// Decode stream (slice, grp, span sp) of object o into dst (slice base).
+// Output rows of one (layer, K/V) slice for the lane's channel.  Row k of a
+// group is token t + k; seek() places t, advance() moves it on.  C is the
+// row length of the [T][C] layout (a compile-time constant where known).
+// [L][2][T][C] layout, shifted by a token offset (chunk destinations).
+struct LinearOut {
+    uint16_t *base;  // token 0 of the slice, lane's channel
+    int64_t shift;   // destination token = object token + shift
+    uint16_t *p;
+    __device__ __forceinline__ void seek(uint32_t tok, uint32_t C) { p = base + ((int64_t)tok + shift) * (int64_t)C; }
+    __device__ __forceinline__ uint16_t *row(uint32_t k, uint32_t C) const { return p + (size_t)k * C; }
+    __device__ __forceinline__ void advance(uint32_t n, uint32_t C) { p += (size_t)n * C; }
+    __device__ __forceinline__ bool ok() const { return true; }
+};
+
+// Device view of a cg_paged_kv destination.
+struct PagedDst {
+    uint16_t *pool;
+    const uint32_t *table;
+    uint32_t n_blocks, n_pool, bshift;
+    uint64_t layer_stride, kv_stride, block_stride, token_stride;
+};
+
+// Paged layout: token t lives in block table[t >> bshift], row t & mask.
+// A group (at most G <= block_tokens rows) touches at most two blocks, whose
+// bases are looked up when the group starts.  A physical block outside the
+// pool stops the span (ok() turns false) before anything is written there.
+struct PagedOut {
+    uint16_t *slice;  // pool + layer and K/V offsets + lane's channel
+    const uint32_t *table;
+    uint32_t n_blocks, n_pool, bshift;
+    uint64_t block_stride, ts;
+    uint32_t t;
+    uint16_t *b0, *b1;
+    bool good;
+    __device__ __forceinline__ uint16_t *block(uint32_t lb) {
+        if (lb >= n_blocks) return slice;  // past the last token: never a row's block
+        const uint32_t pb = table[lb];
+        if (pb >= n_pool) {
+            good = false;
+            return slice;
+        }
+        return slice + (uint64_t)pb * block_stride;
+    }
+    __device__ __forceinline__ void seek(uint32_t tok, uint32_t = 0) {
+        t = tok;
+        b0 = block(t >> bshift);
+        b1 = block((t >> bshift) + 1u);
+    }
+    __device__ __forceinline__ uint16_t *row(uint32_t k, uint32_t = 0) const {
+        const uint32_t u = t + k;
+        return ((u >> bshift) != (t >> bshift) ? b1 : b0) + (uint64_t)(u & ((1u << bshift) - 1u)) * ts;
+    }
+    __device__ __forceinline__ void advance(uint32_t n, uint32_t = 0) { seek(t + n); }
+    __device__ __forceinline__ bool ok() const { return good; }
+};
+
+// Decode stream (slice, grp, span sp) of object o into the rows of `O`.
 // kG = 10 / kC = 1024 select compile-time group size / row stride (0: runtime).
-template <bool kHasEsc, uint32_t kG, uint32_t kC>
+template <bool kHasEsc, uint32_t kG, uint32_t kC, class Out>
 __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice, uint32_t grp, uint32_t sp,
-                                                 float step, const uint8_t *smem, Ring &R, uint16_t *dst_slice,
-                                                 int64_t shift, uint32_t *status, uint64_t sb, uint64_t se,
-                                                 uint32_t eb, uint32_t ee, uint32_t nsteps) {
+                                                 float step, const uint8_t *smem, Ring &R, Out O, uint32_t *status,
+                                                 uint64_t sb, uint64_t se, uint32_t eb, uint32_t ee,
+                                                 uint32_t nsteps) {
     const Geom &g = o.g;
     const uint32_t G = kG ? kG : g.G;
     const uint32_t C = kC ? kC : g.C;
@@ -358,51 +414,51 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
 
     uint32_t p = p0;
     const int8_t *arow = o.anchors + g.anchor_index(slice, c0 + p0) + c;  // row of p0's group
-    uint16_t *out = dst_slice + ((int64_t)(c0 + p0) + shift) * (int64_t)C + c;
+    O.seek(c0 + p0, C);
     float xa = __fmul_rn((float)*arow, sa);
     const uint32_t gp0 = p0 % G;
     if (gp0) {  // head: the rest of a group whose anchor lies before the span
         const uint32_t cnt = min(G - gp0, p1 - p);
-        for (uint32_t k = 0; k < cnt && K.alive; k++) {
+        for (uint32_t k = 0; k < cnt && K.alive && O.ok(); k++) {
             if (k % kMaxRun == 0) ensure(R, K, pw + kLanes * min(kMaxRun, cnt - k));
-            out[(size_t)k * C] = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
+            *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
         }
         p += cnt;
-        out += (size_t)cnt * C;
+        O.advance(cnt, C);
         arow += C;
     }
     // whole groups: anchor + G - 1 steps with one ring check
     int8_t qa_next = p < p1 ? *arow : 0;
-    while (p + G <= p1 && K.alive) {
+    while (p + G <= p1 && K.alive && O.ok()) {
         xa = __fmul_rn((float)qa_next, sa);
         if (p + G < p1) qa_next = arow[C];  // prefetch the next group's anchor
-        out[0] = to_half(xa);
+        *O.row(0, C) = to_half(xa);
         if (kG) ensure(R, K, pw + kLanes * (kG - 1u));  // kG - 1 <= kMaxRun
         if (kG) {
             uint32_t k = 1;
 #pragma unroll
             for (; k < (kG ? kG : 1u); k++)
-                if (!fast_step<kHasEsc>(x, pw, T, ring, xa, out + (size_t)k * C)) break;
+                if (!fast_step<kHasEsc>(x, pw, T, ring, xa, O.row(k, C))) break;
 #pragma unroll 1
             for (; k < (kG ? kG : 1u); k++)
-                out[(size_t)k * C] = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
+                *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
         } else {
             for (uint32_t k = 1; k < G; k++) {
                 if ((k - 1u) % kMaxRun == 0) ensure(R, K, pw + kLanes * min(kMaxRun, G - k));
-                out[(size_t)k * C] = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
+                *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
             }
         }
         p += G;
-        out += (size_t)G * C;
+        O.advance(G, C);
         arow += C;
     }
-    if (p < p1 && K.alive) {  // tail: a group cut by the span end
+    if (p < p1 && K.alive && O.ok()) {  // tail: a group cut by the span end
         xa = __fmul_rn((float)qa_next, sa);
-        out[0] = to_half(xa);
+        *O.row(0, C) = to_half(xa);
         const uint32_t cnt = p1 - p - 1u;
         for (uint32_t k = 1; k <= cnt && K.alive; k++) {
             if ((k - 1u) % kMaxRun == 0) ensure(R, K, pw + kLanes * min(kMaxRun, cnt - k + 1u));
-            out[(size_t)k * C] = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
+            *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
         }
     }
     // drain copies still in flight before the ring is reused
@@ -410,6 +466,10 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
     if (!K.alive) {
         if (T.lane == 0) flag_why(status, CG_ERR_TIMEOUT, kWhyWait);
         return false;
+    }
+    if (!O.ok()) {  // a destination block outside the pool: the span stopped
+        if (T.lane == 0) flag(status, CG_ERR_RANGE);
+        return true;
     }
     uint32_t why = ep == ee ? 0u : kWhyEscapes;
     if (nsteps) {
@@ -426,8 +486,9 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
 
 // Returns false once a bounded wait of this warp has given up: the warp's
 // ring state is then unknown and it takes no further stream.
+template <class Out>
 __device__ bool decode_span(const DecObj &o, uint32_t slice, uint32_t grp, uint32_t sp, float step,
-                            const uint8_t *smem, Ring &R, uint16_t *dst_slice, int64_t shift, uint32_t *status) {
+                            const uint8_t *smem, Ring &R, Out O, uint32_t *status) {
     const Geom &g = o.g;
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t ch = sp / g.spans_full, span = sp - ch * g.spans_full;
@@ -445,7 +506,7 @@ __device__ bool decode_span(const DecObj &o, uint32_t slice, uint32_t grp, uint3
         return true;
     }
 #define CG_SPAN(E, GG, CC) \
-    decode_span_impl<E, GG, CC>(o, slice, grp, sp, step, smem, R, dst_slice, shift, status, sb, se, eb, ee, nsteps)
+    decode_span_impl<E, GG, CC>(o, slice, grp, sp, step, smem, R, O, status, sb, se, eb, ee, nsteps)
     if (g.G == 10 && g.C == 1024) return ee != eb ? CG_SPAN(true, 10, 1024) : CG_SPAN(false, 10, 1024);
     if (g.G == 10) return ee != eb ? CG_SPAN(true, 10, 0) : CG_SPAN(false, 10, 0);
     return ee != eb ? CG_SPAN(true, 0, 0) : CG_SPAN(false, 0, 0);
@@ -468,18 +529,37 @@ __device__ __forceinline__ Ring make_ring(uint8_t *smem, uint32_t nwarps) {
     return R;
 }
 
-__global__ void __maxnreg__(kDecRegs) k_decode_all(DecObj o, StepTable st, uint16_t *out,
-                                                                      uint32_t *status) {
+// kPaged: rows go to the blocks of `pd`, else to out[L][2][T][C].
+template <bool kPaged>
+__global__ void __maxnreg__(kDecRegs) k_decode_all(DecObj o, StepTable st, uint16_t *out, PagedDst pd,
+                                                   uint32_t *status) {
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t grp = blockIdx.x, slice = blockIdx.y, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const uint32_t c = grp * kLanes + (threadIdx.x & 31u);
     const float step = st.v[slice >> 1];
     Ring R = make_ring(smem, nw);
     if (warp == 0) build_tables(o, slice, grp, step, smem, status);
     __syncthreads();
     if (*reinterpret_cast<const int *>(smem + kBadOff)) return;
-    uint16_t *dst = out + (uint64_t)slice * o.g.T * o.g.C;
-    for (uint64_t sp = warp; sp < o.g.spans_total; sp += nw)
-        if (!decode_span(o, slice, grp, (uint32_t)sp, step, smem, R, dst, 0, status)) break;
+    for (uint64_t sp = warp; sp < o.g.spans_total; sp += nw) {
+        bool alive;
+        if (kPaged) {
+            PagedOut O;
+            O.slice = pd.pool + (uint64_t)(slice >> 1) * pd.layer_stride + (uint64_t)(slice & 1u) * pd.kv_stride + c;
+            O.table = pd.table;
+            O.n_blocks = pd.n_blocks;
+            O.n_pool = pd.n_pool;
+            O.bshift = pd.bshift;
+            O.block_stride = pd.block_stride;
+            O.ts = pd.token_stride;
+            O.good = true;
+            alive = decode_span(o, slice, grp, (uint32_t)sp, step, smem, R, O, status);
+        } else {
+            const LinearOut O{out + (uint64_t)slice * o.g.T * o.g.C + c, 0, nullptr};
+            alive = decode_span(o, slice, grp, (uint32_t)sp, step, smem, R, O, status);
+        }
+        if (!alive) break;
+    }
 }
 
 __global__ void __maxnreg__(kDecRegs) k_decode_jobs(const DecObj *objs, const DecJob *jobs,
@@ -497,16 +577,19 @@ __global__ void __maxnreg__(kDecRegs) k_decode_jobs(const DecObj *objs, const De
     for (uint32_t i = warp; i < job.span_count; i += nw) {
         const SpanRef sr = spans[job.span_begin + i];
         const RefDst rd = refs[sr.ref];
-        if (!decode_span(o, job.slice, job.grp, sr.span, step, smem, R,
-                         rd.dst + (uint64_t)job.slice * rd.dst_tokens * o.g.C, rd.shift, status))
-            break;
+        const LinearOut O{rd.dst + (uint64_t)job.slice * rd.dst_tokens * o.g.C + job.grp * kLanes + (threadIdx.x & 31u),
+                          rd.shift, nullptr};
+        if (!decode_span(o, job.slice, job.grp, sr.span, step, smem, R, O, status)) break;
     }
 }
 
 static cudaError_t set_smem_attrs() {
     static cudaError_t err = [] {
-        cudaError_t e = cudaFuncSetAttribute(k_decode_all, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(k_decode_all<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)dec_smem_bytes(kMaxDecWarps));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_decode_all<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)dec_smem_bytes(kMaxDecWarps));
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_decode_jobs, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)dec_smem_bytes(kMaxDecWarps));
@@ -620,8 +703,36 @@ extern "C" cg_status cg_decode(const cg_config *cfg, const cg_encoded *enc, uint
     const dim3 grid(o.g.NG, o.g.n_slices);
     CG_CUDA_TRY(set_smem_attrs());
     const uint32_t nwarps = warps_for(o.g.spans_total);
-    k_decode_all<<<grid, nwarps * 32, dec_smem_bytes(nwarps), static_cast<cudaStream_t>(stream)>>>(o, st, kv_out,
-                                                                                                  dev_status);
+    k_decode_all<false><<<grid, nwarps * 32, dec_smem_bytes(nwarps), static_cast<cudaStream_t>(stream)>>>(
+        o, st, kv_out, PagedDst{}, dev_status);
+    CG_CUDA_TRY(cudaGetLastError());
+    return CG_OK;
+}
+
+extern "C" cg_status cg_decode_paged(const cg_config *cfg, const cg_encoded *enc, const cg_paged_kv *dst,
+                                     uint32_t *dev_status, void *stream) {
+    DecObj o;
+    if (!fill_obj(cfg, enc, &o) || !dst || !dst->pool || !dst->block_table) return CG_ERR_INVALID_ARG;
+    const uint32_t bt = dst->block_tokens;
+    if (bt == 0 || (bt & (bt - 1u)) || bt < o.g.G || dst->n_pool_blocks == 0) return CG_ERR_INVALID_ARG;
+    if ((uint64_t)dst->n_blocks * bt < o.g.T) return CG_ERR_INVALID_ARG;
+    PagedDst pd;
+    pd.pool = dst->pool;
+    pd.table = dst->block_table;
+    pd.n_blocks = dst->n_blocks;
+    pd.n_pool = dst->n_pool_blocks;
+    pd.bshift = (uint32_t)__builtin_ctz(bt);
+    pd.layer_stride = dst->layer_stride;
+    pd.kv_stride = dst->kv_stride;
+    pd.block_stride = dst->block_stride;
+    pd.token_stride = dst->token_stride;
+    StepTable st;
+    for (uint32_t l = 0; l < o.g.L; l++) st.v[l] = cfg->step[l];
+    const dim3 grid(o.g.NG, o.g.n_slices);
+    CG_CUDA_TRY(set_smem_attrs());
+    const uint32_t nwarps = warps_for(o.g.spans_total);
+    k_decode_all<true><<<grid, nwarps * 32, dec_smem_bytes(nwarps), static_cast<cudaStream_t>(stream)>>>(
+        o, st, nullptr, pd, dev_status);
     CG_CUDA_TRY(cudaGetLastError());
     return CG_OK;
 }

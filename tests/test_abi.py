@@ -170,3 +170,16 @@ def test_decode_chunks_plan_sizes_on_host():
         C.cg_decode_chunks_ws_bytes([C.ChunkRef(pc, enc, 4, dst, 0)])
     with pytest.raises(C.CodecError):  # destination too short for the chunk
         C.cg_decode_chunks_ws_bytes([C.ChunkRef(pc, enc, 0, dst, 800)])
+
+
+@pytest.mark.parametrize("bt,nb", [(12, 100), (8, 200), (16, 62), (0, 100)])
+def test_paged_decode_rejects_bad_layouts_on_host(bt, nb):
+    """block_tokens must be a power of two >= group_size and the blocks must
+    cover T; checked before anything is enqueued (no GPU needed)."""
+    pc, _ = P.configs(2, 1000, 64, 10, 0, 128)
+    enc = C.alloc_encoded(pc, device="cpu")
+    pool = torch.empty(1 << 16, dtype=torch.float16)
+    table = torch.zeros(nb, dtype=torch.int32)
+    with pytest.raises(C.CodecError) as e:
+        C.cg_decode_paged(pc, enc, pool, table, bt, 0, 0, 0, 64, torch.zeros(1, dtype=torch.int32))
+    assert e.value.code == C.CG_ERR_INVALID_ARG

@@ -287,3 +287,61 @@ def test_full_size_mistral7b_mixed_levels():
                     continue
                 sl = slice(ch * w.chunk_tokens, min(w.T, (ch + 1) * w.chunk_tokens))
                 assert np.array_equal(got[:, :, sl], odec[:, :, sl]), f"chunk {ch} x{m} layers {l0}:{l1}"
+
+
+def _paged(layout, L, npool, bt, Cc):
+    """Pool shape and (layer, K/V, block, token) strides of two paged layouts."""
+    if layout == "layer_major":  # [L][n_pool][2][bt][C]
+        return (L, npool, 2, bt, Cc), dict(layer_stride=npool * 2 * bt * Cc, block_stride=2 * bt * Cc,
+                                           kv_stride=bt * Cc, token_stride=Cc)
+    return (npool, L, 2, bt, Cc), dict(layer_stride=2 * bt * Cc, block_stride=L * 2 * bt * Cc,  # [n_pool][L][2][bt][C]
+                                       kv_stride=bt * Cc, token_stride=Cc)
+
+
+@needs_gpu
+@pytest.mark.parametrize("layout,bt", [("layer_major", 16), ("block_major", 32), ("layer_major", 1024)])
+def test_paged_decode_matches_oracle(layout, bt):
+    """Decode straight into a paged block pool through a shuffled block table:
+    gathering the blocks back gives the oracle's cache bit for bit, and the
+    pool's unused blocks and the rows past the last token stay untouched."""
+    L, T, Cc = 3, 1000, 64
+    x = synth.ar1_kv(L, T, Cc, 0.9, 2, seed=51)
+    x[1, 0, 37, 5] = 30000.0  # an escape
+    pc, oc = P.configs(L, T, Cc, 10, 0, 128)
+    odec = O.decode(oc, O.encode(oc, x.numpy().view(np.uint16)))
+    enc = C.encode(pc, x.cuda())
+    nb = (T + bt - 1) // bt
+    npool = nb + 5
+    perm = np.random.default_rng(bt).permutation(npool)[:nb]
+    table = torch.tensor(perm, dtype=torch.int32, device="cuda")
+    shape, st = _paged(layout, L, npool, bt, Cc)
+    pool = torch.full(shape, -1, dtype=torch.int16, device="cuda")  # 0xFFFF: never a decoded value
+    status = C.new_status()
+    C.cg_decode_paged(pc, enc, pool.view(torch.float16).view(-1), table, bt, status=status, n_pool_blocks=npool, **st)
+    torch.cuda.synchronize()
+    assert C.read_status(status) == C.CG_OK
+    P16 = pool.cpu().numpy().view(np.uint16)
+    blk = (lambda pb: P16[:, pb]) if layout == "layer_major" else (lambda pb: P16[pb])
+    got = np.concatenate([blk(pb) for pb in perm], axis=2)  # [L][2][nb * bt][C]
+    assert np.array_equal(got[:, :, :T], odec)
+    assert (got[:, :, T:] == 0xFFFF).all()
+    for pb in sorted(set(range(npool)) - set(perm.tolist())):
+        assert (blk(pb) == 0xFFFF).all()
+
+
+@needs_gpu
+def test_paged_decode_block_outside_pool_is_flagged_not_written():
+    L, T, Cc, bt = 2, 300, 32, 16
+    pc, _ = P.configs(L, T, Cc, 10, 0, 128)
+    enc = C.encode(pc, synth.ar1_kv(L, T, Cc, 0.9, 1, seed=52).cuda())
+    nb = (T + bt - 1) // bt
+    npool = nb
+    table = torch.arange(nb, dtype=torch.int32, device="cuda")
+    table[7] = npool  # points at the guard block past the pool
+    shape, st = _paged("block_major", L, npool + 1, bt, Cc)
+    pool = torch.full(shape, -1, dtype=torch.int16, device="cuda")
+    status = C.new_status()
+    C.cg_decode_paged(pc, enc, pool.view(torch.float16).view(-1), table, bt, status=status, n_pool_blocks=npool, **st)
+    torch.cuda.synchronize()
+    assert C.read_status(status) == C.CG_ERR_RANGE
+    assert (pool[npool].cpu().numpy().view(np.uint16) == 0xFFFF).all()
