@@ -157,6 +157,24 @@ cg_status cg_encode(const cg_config *cfg, const uint16_t *kv, void *ws, size_t w
                     cg_sizes *sizes, uint32_t *dev_status, void *stream);
 
 /*
+ * Encode one cache at several quality levels in one call (at most 4): level
+ * l uses cfg->step[k] * mult[l] for layer k, the way the CacheGen pages keep
+ * every chunk at a high, medium and low quality ("CacheGen vs 传统量化KV缓存
+ * 压缩技术深度对比与性能测试", §2.2).  One statistics pass reads the cache once
+ * for every level: anchors and scales (the same at every level) and each
+ * level's tables.  The levels are then coded and packed one after another
+ * in one shared scratch region.  outs[l] / sizes[l] are level l's object and
+ * sizes, each exactly what cg_encode gives with the level's steps.  outs[l]
+ * may share the anchors and scales buffers of outs[0]; otherwise they get a
+ * copy.  Every level's steps must be valid steps (> 2^-10, finite).
+ *   ws: device, cg_encode_levels_ws_bytes() bytes, 256-byte aligned.
+ */
+cg_status cg_encode_levels_ws_bytes(const cg_config *cfg, uint32_t n_levels, size_t *ws_bytes);
+cg_status cg_encode_levels(const cg_config *cfg, uint32_t n_levels, const float *mult, const uint16_t *kv, void *ws,
+                           size_t ws_bytes, const cg_encoded *outs, cg_sizes *sizes, uint32_t *dev_status,
+                           void *stream);
+
+/*
  * Decode a whole encoded object (device pointers in *enc) into kv_out
  * (device, fp16 bits, [L][2][T][C]).  One thread block per (layer, K/V,
  * 32-channel group) loads its 32 frequency tables into shared memory; each

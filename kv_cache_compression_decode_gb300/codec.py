@@ -92,7 +92,8 @@ class cg_chunk_time(ct.Structure):
 EXPORTS = ("cg_status_string", "cg_status_from_flags", "cg_encode_bounds", "cg_encode", "cg_decode",
            "cg_decode_chunks_ws_bytes", "cg_decode_chunks", "cg_decode_chunks_noalloc", "cg_chunk_ranges",
            "cg_serialize",
-           "cg_deserialize_header", "cg_deserialize", "cg_plan_levels", "cg_decode_paged")
+           "cg_deserialize_header", "cg_deserialize", "cg_plan_levels", "cg_decode_paged",
+           "cg_encode_levels_ws_bytes", "cg_encode_levels")
 
 _lib = None
 
@@ -119,6 +120,8 @@ def lib() -> ct.CDLL:
         L.cg_deserialize_header.argtypes = [P, ct.c_size_t, ct.POINTER(cg_config), P, ct.POINTER(cg_sizes)]
         L.cg_deserialize.argtypes = [P, ct.c_size_t, ct.POINTER(cg_encoded)]
         L.cg_plan_levels.argtypes = [ct.POINTER(cg_level_plan), P, P, ct.POINTER(ct.c_double)]
+        L.cg_encode_levels_ws_bytes.argtypes = [ct.POINTER(cg_config), U32, ct.POINTER(ct.c_size_t)]
+        L.cg_encode_levels.argtypes = [ct.POINTER(cg_config), U32, P, P, P, ct.c_size_t, P, P, P, P]
         L.cg_decode_paged.argtypes = [ct.POINTER(cg_config), ct.POINTER(cg_encoded), ct.POINTER(cg_paged_kv), P, P]
         for name in EXPORTS:
             if name not in ("cg_status_string",):
@@ -460,6 +463,54 @@ def encode(cfg: Config, kv: torch.Tensor, stream=None) -> Encoded:
         st = read_status(enc.status)
     _check(st, "cg_encode (device)")
     return enc.result()
+
+
+def cg_encode_levels_ws_bytes(cfg: Config, n_levels: int) -> int:
+    n = ct.c_size_t()
+    _check(lib().cg_encode_levels_ws_bytes(ct.byref(cfg.c()), n_levels, ct.byref(n)), "cg_encode_levels_ws_bytes")
+    return int(n.value)
+
+
+def encode_levels(cfg: Config, kv: torch.Tensor, mults: Sequence[float], share_anchors: bool = True,
+                  stream=None) -> List[Tuple[Config, Encoded]]:
+    """Encode a device cache at len(mults) quality levels with one call (one
+    statistics pass over the cache); level l uses cfg.step * mults[l].
+    Returns (level config, trimmed object) per level; each object equals
+    encode() with that level's steps.  With share_anchors the levels' objects
+    share one anchors and one scales buffer."""
+    dev = kv.device
+    n = len(mults)
+    m32 = np.ascontiguousarray(mults, dtype=np.float32)
+    cfgs = [Config(cfg.L, cfg.T, cfg.C, cfg.group_size, cfg.chunk_tokens, cfg.tokens_per_stream,
+                   (np.asarray(cfg.step, np.float32) * m).astype(np.float32)) for m in m32]
+    ws = torch.empty(cg_encode_levels_ws_bytes(cfg, n), dtype=torch.uint8, device=dev)
+    sizes_buf = torch.zeros(4 * n, dtype=torch.int64, pin_memory=True)
+    sizes = (cg_sizes * n).from_address(sizes_buf.data_ptr())
+    esc_cap = None
+    for _ in range(2):
+        outs = [alloc_encoded(cfg, dev, esc_cap) for _ in range(n)]
+        if share_anchors:
+            for o in outs[1:]:
+                o.anchors, o.scales = outs[0].anchors, outs[0].scales
+        arr = (cg_encoded * n)(*[o.c() for o in outs])
+        status = new_status(dev)
+        code = lib().cg_encode_levels(ct.byref(cfg.c()), n, m32.ctypes.data, kv.data_ptr(), ws.data_ptr(), ws.numel(),
+                                      arr, ct.addressof(sizes), status.data_ptr(), _stream_ptr(stream))
+        _check(code, "cg_encode_levels")
+        torch.cuda.synchronize(dev)
+        st = read_status(status)
+        need = max(int(sz.n_escapes) for sz in sizes)
+        if st == CG_ERR_RANGE and need > outs[0].escapes.numel():
+            esc_cap = need
+            continue
+        _check(st, "cg_encode_levels (device)")
+        break
+    res = []
+    for c, o, sz in zip(cfgs, outs, sizes):
+        o.sizes = {"payload_bytes": int(sz.payload_bytes), "tables_bytes": int(sz.tables_bytes),
+                   "n_escapes": int(sz.n_escapes), "total_bytes": int(sz.total_bytes)}
+        res.append((c, o.trimmed()))
+    return res
 
 
 def decode(cfg: Config, enc: Encoded, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:

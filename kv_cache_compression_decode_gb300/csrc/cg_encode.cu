@@ -50,12 +50,28 @@ struct EncArgs {
     uint32_t *status;
 };
 
-// Workspace carving (256-byte aligned pieces).
-struct WsLayout {
-    uint64_t ftab, tlohi, twidth, esc_count, words_count, scratch, dsizes, total, region_words;
+// Quality levels one multi-level encode can produce (the pages store each
+// chunk at three: "CacheGen vs 传统量化KV缓存压缩技术深度对比与性能测试", §2.2).
+constexpr uint32_t kMaxLevels = 4;
+
+// Per-level outputs of the statistics pass: a multi-level encode counts the
+// symbols of every level in one read of the cache.  Level l quantizes with
+// the layer's step times mult[l].
+struct StatsLevels {
+    uint16_t *ftab[kMaxLevels];
+    uint32_t *tlohi[kMaxLevels], *twidth[kMaxLevels], *esc_count[kMaxLevels];
+    float mult[kMaxLevels];
 };
 
-static WsLayout ws_layout(const Geom &g) {
+// Workspace carving (256-byte aligned pieces): per-level tables and counts,
+// one scratch region shared by the levels (they are coded one after another).
+struct WsLayout {
+    uint64_t ftab[kMaxLevels], tlohi[kMaxLevels], twidth[kMaxLevels], esc_count[kMaxLevels],
+        words_count[kMaxLevels], dsizes[kMaxLevels];
+    uint64_t scratch, total, region_words;
+};
+
+static WsLayout ws_layout(const Geom &g, uint32_t levels = 1) {
     WsLayout w;
     uint64_t o = 0;
     auto take = [&](uint64_t bytes) {
@@ -64,13 +80,15 @@ static WsLayout ws_layout(const Geom &g) {
         return at;
     };
     w.region_words = round_up((uint64_t)kLanes * (g.tps + 2u), 8);
-    w.ftab = take(g.n_tables * 256u * 2u);
-    w.tlohi = take(g.n_tables * 4u);
-    w.twidth = take(g.n_tables * 4u);
-    w.esc_count = take(g.n_streams * 4u);
-    w.words_count = take(g.n_streams * 4u);
+    for (uint32_t l = 0; l < levels; l++) {
+        w.ftab[l] = take(g.n_tables * 256u * 2u);
+        w.tlohi[l] = take(g.n_tables * 4u);
+        w.twidth[l] = take(g.n_tables * 4u);
+        w.esc_count[l] = take(g.n_streams * 4u);
+        w.words_count[l] = take(g.n_streams * 4u);
+        w.dsizes[l] = take(sizeof(cg_sizes));
+    }
     w.scratch = take(g.n_streams * w.region_words * 2u);
-    w.dsizes = take(sizeof(cg_sizes));
     w.total = o;
     return w;
 }
@@ -107,10 +125,25 @@ __device__ __forceinline__ uint32_t anchor_token(const Geom &g, uint32_t r) {
 
 // Quantize one group's anchor and deltas and count the delta symbols.
 // v[0] is the anchor token's value, v[1..N-1] the deltas' (already loaded).
-template <uint32_t N>
-__device__ __forceinline__ void stats_full_group(const EncArgs &a, uint32_t slice, uint32_t grp, uint32_t ch,
-                                                 uint32_t c0, uint32_t p0, const float (&v)[N], float sa, float inv_sa,
-                                                 float inv_step, uint32_t *hist, bool &nonfinite) {
+// Symbol of delta d at each level: count it in that level's histogram
+// (hist + level * 256 * 32) and, for an escape, in the stream's count.
+template <uint32_t NL>
+__device__ __forceinline__ void count_delta(const EncArgs &a, const StatsLevels &lv, float d, const float (&inv_step)[NL],
+                                            uint32_t *hist, uint32_t lane, uint64_t stream) {
+#pragma unroll
+    for (uint32_t l = 0; l < NL; l++) {
+        const int q = __float2int_rn(__fmul_rn(d, inv_step[l]));
+        const uint32_t s = symbol_of(q);
+        atomicAdd(&hist[l * 256u * kLanes + s * kLanes + lane], 1u);
+        if (s == kEsc) atomicAdd(&lv.esc_count[l][stream], 1u);
+    }
+}
+
+template <uint32_t N, uint32_t NL>
+__device__ __forceinline__ void stats_full_group(const EncArgs &a, const StatsLevels &lv, uint32_t slice, uint32_t grp,
+                                                 uint32_t ch, uint32_t c0, uint32_t p0, const float (&v)[N], float sa,
+                                                 float inv_sa, const float (&inv_step)[NL], uint32_t *hist,
+                                                 bool &nonfinite) {
     const Geom &g = a.g;
     const uint32_t lane = threadIdx.x & 31u, c = grp * kLanes + lane;
     nonfinite |= !isfinite(v[0]);
@@ -120,17 +153,17 @@ __device__ __forceinline__ void stats_full_group(const EncArgs &a, uint32_t slic
 #pragma unroll
     for (uint32_t i = 1; i < N; i++) {
         nonfinite |= !isfinite(v[i]);
-        const int q = __float2int_rn(__fmul_rn(__fsub_rn(v[i], xa), inv_step));
-        const uint32_t s = symbol_of(q);
-        atomicAdd(&hist[s * kLanes + lane], 1u);
-        if (s == kEsc) atomicAdd(&a.esc_count[g.stream_index(ch, slice, (p0 + i) / g.tps, grp)], 1u);
+        count_delta<NL>(a, lv, __fsub_rn(v[i], xa), inv_step, hist, lane,
+                        g.stream_index(ch, slice, (p0 + i) / g.tps, grp));
     }
 }
 
 // Same for a group of any length n (loads inside the loop).
-__device__ __forceinline__ void stats_any_group(const EncArgs &a, uint32_t slice, uint32_t grp, uint32_t ch, uint32_t c0,
-                                             uint32_t p0, uint32_t n, const uint16_t *x, float sa, float inv_sa,
-                                             float inv_step, uint32_t *hist, bool &nonfinite) {
+template <uint32_t NL>
+__device__ __forceinline__ void stats_any_group(const EncArgs &a, const StatsLevels &lv, uint32_t slice, uint32_t grp,
+                                             uint32_t ch, uint32_t c0, uint32_t p0, uint32_t n, const uint16_t *x,
+                                             float sa, float inv_sa, const float (&inv_step)[NL], uint32_t *hist,
+                                             bool &nonfinite) {
     const Geom &g = a.g;
     const uint32_t lane = threadIdx.x & 31u, c = grp * kLanes + lane;
     const uint16_t *xp = x + (uint64_t)(c0 + p0) * g.C;
@@ -142,20 +175,18 @@ __device__ __forceinline__ void stats_any_group(const EncArgs &a, uint32_t slice
     for (uint32_t i = 1; i < n; i++) {
         const float vi = ld_half(xp + (uint64_t)i * g.C);
         nonfinite |= !isfinite(vi);
-        const int q = __float2int_rn(__fmul_rn(__fsub_rn(vi, xa), inv_step));
-        const uint32_t s = symbol_of(q);
-        atomicAdd(&hist[s * kLanes + lane], 1u);
-        if (s == kEsc) atomicAdd(&a.esc_count[g.stream_index(ch, slice, (p0 + i) / g.tps, grp)], 1u);
+        count_delta<NL>(a, lv, __fsub_rn(vi, xa), inv_step, hist, lane,
+                        g.stream_index(ch, slice, (p0 + i) / g.tps, grp));
     }
 }
 
 // All groups of one slice and channel group, warps strided over groups.
 // kG > 0: compile-time group size; two whole groups are loaded before either
 // is processed so that 2 kG row loads are in flight per lane.
-template <uint32_t kG>
-__device__ __forceinline__ void stats_groups(const EncArgs &a, uint32_t slice, uint32_t grp, const uint16_t *x,
-                                             float sa, float inv_sa, float inv_step, uint32_t *hist,
-                                             bool &nonfinite) {
+template <uint32_t kG, uint32_t NL>
+__device__ __forceinline__ void stats_groups(const EncArgs &a, const StatsLevels &lv, uint32_t slice, uint32_t grp,
+                                             const uint16_t *x, float sa, float inv_sa, const float (&inv_step)[NL],
+                                             uint32_t *hist, bool &nonfinite) {
     const Geom &g = a.g;
     const uint32_t warp = threadIdx.x >> 5, A = (uint32_t)g.A;
     for (uint32_t r0 = warp; r0 < A; r0 += 2u * kStatsWarps) {
@@ -186,17 +217,22 @@ __device__ __forceinline__ void stats_groups(const EncArgs &a, uint32_t slice, u
             }
         }
         if (kG && n[0] == kG)
-            stats_full_group(a, slice, grp, ch[0], c0[0], p0[0], v0, sa, inv_sa, inv_step, hist, nonfinite);
+            stats_full_group(a, lv, slice, grp, ch[0], c0[0], p0[0], v0, sa, inv_sa, inv_step, hist, nonfinite);
         else if (n[0])
-            stats_any_group(a, slice, grp, ch[0], c0[0], p0[0], n[0], x, sa, inv_sa, inv_step, hist, nonfinite);
+            stats_any_group(a, lv, slice, grp, ch[0], c0[0], p0[0], n[0], x, sa, inv_sa, inv_step, hist, nonfinite);
         if (kG && n[1] == kG)
-            stats_full_group(a, slice, grp, ch[1], c0[1], p0[1], v1, sa, inv_sa, inv_step, hist, nonfinite);
+            stats_full_group(a, lv, slice, grp, ch[1], c0[1], p0[1], v1, sa, inv_sa, inv_step, hist, nonfinite);
         else if (n[1])
-            stats_any_group(a, slice, grp, ch[1], c0[1], p0[1], n[1], x, sa, inv_sa, inv_step, hist, nonfinite);
+            stats_any_group(a, lv, slice, grp, ch[1], c0[1], p0[1], n[1], x, sa, inv_sa, inv_step, hist, nonfinite);
     }
 }
 
-__global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable st) {
+// NL levels in one pass: their histograms side by side in dynamic shared
+// memory (NL x 32 KB); anchors and scales are the same for every level.
+// (Four blocks per SM for one level: the pass waits on memory, so it wants
+// the resident warps; NL > 1 is held to two by its shared memory anyway.)
+template <uint32_t NL>
+__global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 4 : 2) k_stats(EncArgs a, StepTable st, StatsLevels lv) {
     const Geom &g = a.g;
     const uint32_t grp = blockIdx.x, slice = blockIdx.y;
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
@@ -204,11 +240,11 @@ __global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable
     const uint16_t *x = a.kv + (uint64_t)slice * g.T * g.C + c;
     const float step = st.v[slice >> 1];
 
-    __shared__ uint32_t hist[256 * kLanes];  // [symbol][lane]
+    extern __shared__ __align__(16) uint32_t hist[];  // [level][symbol][lane]
     __shared__ float red[kStatsWarps][kLanes];
     __shared__ float s_scale[kLanes];
 
-    for (uint32_t i = threadIdx.x; i < 256u * kLanes; i += blockDim.x) hist[i] = 0;
+    for (uint32_t i = threadIdx.x; i < NL * 256u * kLanes; i += blockDim.x) hist[i] = 0;
 
     // E1: absmax over this call's anchor rows -> scale = absmax / 127
     // (four independent row loads in flight per lane).
@@ -240,16 +276,24 @@ __global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable
     // E2 + E3 + E4: one warp per group of tokens (anchor + its deltas); the
     // 10-token groups of the CacheGen pipeline load two whole groups at once.
     bool nonfinite = false;
-    const float inv_sa = __fdiv_rn(1.f, sa), inv_step = __fdiv_rn(1.f, step);  // one rounding each
+    const float inv_sa = __fdiv_rn(1.f, sa);  // one rounding each
+    float inv_step[NL];
+#pragma unroll
+    for (uint32_t l = 0; l < NL; l++) inv_step[l] = __fdiv_rn(1.f, __fmul_rn(step, lv.mult[l]));
     if (g.G == 10)
-        stats_groups<10>(a, slice, grp, x, sa, inv_sa, inv_step, hist, nonfinite);
+        stats_groups<10, NL>(a, lv, slice, grp, x, sa, inv_sa, inv_step, hist, nonfinite);
     else
-        stats_groups<0>(a, slice, grp, x, sa, inv_sa, inv_step, hist, nonfinite);
+        stats_groups<0, NL>(a, lv, slice, grp, x, sa, inv_sa, inv_step, hist, nonfinite);
     if (__any_sync(kFull, nonfinite) && lane == 0) flag(a.status, CG_ERR_NONFINITE);
     __syncthreads();
 
-    // E5: normalize each channel's counts to a 16-bit table (warp per channel).
-    for (uint32_t j = warp; j < kLanes; j += kStatsWarps) {
+    // E5: normalize each channel's counts to a 16-bit table (warp per
+    // (level, channel)).
+    for (uint32_t jj = warp; jj < NL * kLanes; jj += kStatsWarps) {
+        const uint32_t lvl = jj / kLanes, j = jj % kLanes;
+        const uint32_t *hl = hist + lvl * 256u * kLanes;
+        uint16_t *ftab = lv.ftab[lvl];
+        uint32_t *tlohi = lv.tlohi[lvl], *twidth = lv.twidth[lvl];
         const uint64_t table = (uint64_t)slice * g.C + grp * kLanes + j;
         uint32_t n[8], f[8];
         uint32_t N = 0, lo = 256, hi = 0;
@@ -257,7 +301,7 @@ __global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable
         #pragma unroll
         for (int i = 0; i < 8; i++) {
             uint32_t s = (uint32_t)i * 32u + lane;
-            n[i] = hist[s * kLanes + j];
+            n[i] = hl[s * kLanes + j];
             N += n[i];
             if (n[i]) {
                 lo = min(lo, s);
@@ -273,8 +317,8 @@ __global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable
         any = __any_sync(kFull, any);
         if (!any) {
             if (lane == 0) {
-                a.tlohi[table] = 1u;
-                a.twidth[table] = 2u;
+                tlohi[table] = 1u;
+                twidth[table] = 2u;
             }
             continue;
         }
@@ -324,11 +368,11 @@ __global__ void __launch_bounds__(kStatsWarps * 32) k_stats(EncArgs a, StepTable
         #pragma unroll
         for (int i = 0; i < 8; i++) {
             uint32_t s = (uint32_t)i * 32u + lane;
-            if (s >= lo && s <= hi) a.ftab[table * 256u + s] = (uint16_t)(f[i] - 1u);
+            if (s >= lo && s <= hi) ftab[table * 256u + s] = (uint16_t)(f[i] - 1u);
         }
         if (lane == 0) {
-            a.tlohi[table] = lo | (hi << 8);
-            a.twidth[table] = 2u + 2u * (hi - lo + 1u);
+            tlohi[table] = lo | (hi << 8);
+            twidth[table] = 2u + 2u * (hi - lo + 1u);
         }
     }
 }
@@ -597,68 +641,137 @@ extern "C" cg_status cg_encode_bounds(const cg_config *cfg, cg_bounds *b) {
     return CG_OK;
 }
 
-extern "C" cg_status cg_encode(const cg_config *cfg, const uint16_t *kv, void *ws, size_t ws_bytes,
-                               const cg_encoded *out, cg_sizes *sizes, uint32_t *dev_status, void *stream) {
+static bool outputs_ok(const cg_encoded *out) {
+    return out && out->anchors && out->scales && out->tables && out->table_off && out->stream_off && out->esc_off &&
+           (out->payload || !out->payload_cap) && (out->escapes || !out->escapes_cap) &&
+           reinterpret_cast<uintptr_t>(out->payload) % 16u == 0;
+}
+
+template <uint32_t NL>
+static cudaError_t launch_stats(dim3 grid, cudaStream_t s, const EncArgs &a, const StepTable &st, const StatsLevels &lv) {
+    constexpr int bytes = (int)(NL * 256u * kLanes * 4u);
+    static const cudaError_t attr =
+        cudaFuncSetAttribute(k_stats<NL>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (attr != cudaSuccess) return attr;
+    k_stats<NL><<<grid, kStatsWarps * 32, bytes, s>>>(a, st, lv);
+    return cudaGetLastError();
+}
+
+// The encode of `levels` quality levels of one cache: level l uses the
+// configured steps times mult[l].  One statistics pass reads the cache for
+// every level (anchors, scales and all levels' tables); then each level is
+// coded and packed in turn, sharing the scratch region.  Level 0 receives
+// the anchors and scales; a later level whose sections are other buffers
+// gets a copy.
+static cg_status encode_levels(const cg_config *cfg, uint32_t levels, const float *mult, const uint16_t *kv, void *ws,
+                               size_t ws_bytes, const cg_encoded *outs, cg_sizes *sizes, uint32_t *dev_status,
+                               void *stream) {
     Geom g;
-    if (!make_geom(cfg, &g)) return CG_ERR_INVALID_ARG;
-    if (!kv || !ws || !out || !sizes || !out->anchors || !out->scales || !out->tables || !out->table_off ||
-        !out->stream_off || !out->esc_off || (!out->payload && out->payload_cap) ||
-        (!out->escapes && out->escapes_cap))
-        return CG_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(ws) % 256u || reinterpret_cast<uintptr_t>(out->payload) % 16u)
-        return CG_ERR_INVALID_ARG;
+    if (!make_geom(cfg, &g) || levels == 0 || levels > kMaxLevels || !mult) return CG_ERR_INVALID_ARG;
+    if (!kv || !ws || !outs || !sizes || reinterpret_cast<uintptr_t>(ws) % 256u) return CG_ERR_INVALID_ARG;
+    for (uint32_t l = 0; l < levels; l++) {
+        if (!outputs_ok(&outs[l]) || !(mult[l] > 0.f) || !isfinite(mult[l])) return CG_ERR_INVALID_ARG;
+        for (uint32_t k = 0; k < g.L; k++) {  // every level's steps must be valid steps
+            const float st = cfg->step[k] * mult[l];
+            if (!(st > 1.0f / 1024.0f) || !(st < 3e38f)) return CG_ERR_INVALID_ARG;
+        }
+    }
     cg_bounds bd;
     cg_status bs = cg_encode_bounds(cfg, &bd);
     if (bs != CG_OK) return bs;
-    if (ws_bytes < bd.workspace_bytes) return CG_ERR_RANGE;
-    const WsLayout L = ws_layout(g);
+    const WsLayout L = ws_layout(g, levels);
+    if (ws_bytes < L.total) return CG_ERR_RANGE;
     uint8_t *w = static_cast<uint8_t *>(ws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    EncArgs a;
-    a.g = g;
-    a.kv = kv;
-    a.anchors = out->anchors;
-    a.scales = out->scales;
-    a.tables = out->tables;
-    a.table_off = out->table_off;
-    a.payload = out->payload;
-    a.stream_off = out->stream_off;
-    a.escapes = out->escapes;
-    a.esc_off = out->esc_off;
-    a.tables_cap = out->tables_cap;
-    a.payload_cap = out->payload_cap;
-    a.escapes_cap = out->escapes_cap;
-    a.ftab = reinterpret_cast<uint16_t *>(w + L.ftab);
-    a.tlohi = reinterpret_cast<uint32_t *>(w + L.tlohi);
-    a.twidth = reinterpret_cast<uint32_t *>(w + L.twidth);
-    a.esc_count = reinterpret_cast<uint32_t *>(w + L.esc_count);
-    a.words_count = reinterpret_cast<uint32_t *>(w + L.words_count);
-    a.scratch = reinterpret_cast<uint16_t *>(w + L.scratch);
-    a.region_words = L.region_words;
-    a.dsizes = reinterpret_cast<cg_sizes *>(w + L.dsizes);
-    a.status = dev_status;
-
+    auto args = [&](uint32_t l) {
+        const cg_encoded *out = &outs[l];
+        EncArgs a;
+        a.g = g;
+        a.kv = kv;
+        a.anchors = out->anchors;
+        a.scales = out->scales;
+        a.tables = out->tables;
+        a.table_off = out->table_off;
+        a.payload = out->payload;
+        a.stream_off = out->stream_off;
+        a.escapes = out->escapes;
+        a.esc_off = out->esc_off;
+        a.tables_cap = out->tables_cap;
+        a.payload_cap = out->payload_cap;
+        a.escapes_cap = out->escapes_cap;
+        a.ftab = reinterpret_cast<uint16_t *>(w + L.ftab[l]);
+        a.tlohi = reinterpret_cast<uint32_t *>(w + L.tlohi[l]);
+        a.twidth = reinterpret_cast<uint32_t *>(w + L.twidth[l]);
+        a.esc_count = reinterpret_cast<uint32_t *>(w + L.esc_count[l]);
+        a.words_count = reinterpret_cast<uint32_t *>(w + L.words_count[l]);
+        a.scratch = reinterpret_cast<uint16_t *>(w + L.scratch);
+        a.region_words = L.region_words;
+        a.dsizes = reinterpret_cast<cg_sizes *>(w + L.dsizes[l]);
+        a.status = dev_status;
+        return a;
+    };
+    StatsLevels lv;
+    for (uint32_t l = 0; l < kMaxLevels; l++) {
+        const EncArgs a = args(l < levels ? l : 0);
+        lv.ftab[l] = a.ftab;
+        lv.tlohi[l] = a.tlohi;
+        lv.twidth[l] = a.twidth;
+        lv.esc_count[l] = a.esc_count;
+        lv.mult[l] = l < levels ? mult[l] : 1.f;
+        if (l < levels) CG_CUDA_TRY(cudaMemsetAsync(a.esc_count, 0, g.n_streams * 4u, s));
+    }
     StepTable st;
-    for (uint32_t l = 0; l < g.L; l++) st.v[l] = cfg->step[l];
-
+    for (uint32_t k = 0; k < g.L; k++) st.v[k] = cfg->step[k];
     const dim3 grid(g.NG, g.n_slices);
-    CG_CUDA_TRY(cudaMemsetAsync(a.esc_count, 0, g.n_streams * 4u, s));
-    k_stats<<<grid, kStatsWarps * 32, 0, s>>>(a, st);
-    k_scan<uint32_t, false><<<1, 1024, 0, s>>>(a.twidth, g.n_tables, a.table_off, a.tables_cap, a.status);
-    k_scan<uint32_t, false><<<1, 1024, 0, s>>>(a.esc_count, g.n_streams, a.esc_off, a.escapes_cap, a.status);
-    const uint32_t enc_warps = (uint32_t)(g.spans_total < (uint64_t)kMaxEncWarps ? g.spans_total : kMaxEncWarps);
+    const EncArgs a0 = args(0);
+    cudaError_t e = levels == 1 ? launch_stats<1>(grid, s, a0, st, lv)
+                    : levels == 2 ? launch_stats<2>(grid, s, a0, st, lv)
+                    : levels == 3 ? launch_stats<3>(grid, s, a0, st, lv)
+                                  : launch_stats<4>(grid, s, a0, st, lv);
+    CG_CUDA_TRY(e);
     static const cudaError_t attr =
         cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEncSmemBytes);
     CG_CUDA_TRY(attr);
-    k_encode<<<grid, enc_warps * 32, kEncSmemBytes, s>>>(a, st);
-    k_scan<uint64_t, true><<<1, 1024, 0, s>>>(a.words_count, g.n_streams, a.stream_off, a.payload_cap, a.status);
-    const uint64_t pack_blocks = (g.n_streams * 32u + 255u) / 256u;
-    k_pack<<<(unsigned)pack_blocks, 256, 0, s>>>(a);
+    const uint32_t enc_warps = (uint32_t)(g.spans_total < (uint64_t)kMaxEncWarps ? g.spans_total : kMaxEncWarps);
     const uint64_t fixed = bd.anchors_bytes + bd.scales_bytes + bd.table_off_bytes + bd.stream_off_bytes +
                            bd.esc_off_bytes;
-    k_sizes<<<1, 1, 0, s>>>(a, fixed);
-    CG_CUDA_TRY(cudaGetLastError());
-    CG_CUDA_TRY(cudaMemcpyAsync(sizes, a.dsizes, sizeof(cg_sizes), cudaMemcpyDeviceToHost, s));
+    for (uint32_t l = 0; l < levels; l++) {
+        const EncArgs a = args(l);
+        StepTable stl;
+        for (uint32_t k = 0; k < g.L; k++) stl.v[k] = cfg->step[k] * mult[l];
+        if (l > 0 && a.anchors != a0.anchors)
+            CG_CUDA_TRY(cudaMemcpyAsync(a.anchors, a0.anchors, bd.anchors_bytes, cudaMemcpyDeviceToDevice, s));
+        if (l > 0 && a.scales != a0.scales)
+            CG_CUDA_TRY(cudaMemcpyAsync(a.scales, a0.scales, bd.scales_bytes, cudaMemcpyDeviceToDevice, s));
+        k_scan<uint32_t, false><<<1, 1024, 0, s>>>(a.twidth, g.n_tables, a.table_off, a.tables_cap, a.status);
+        k_scan<uint32_t, false><<<1, 1024, 0, s>>>(a.esc_count, g.n_streams, a.esc_off, a.escapes_cap, a.status);
+        k_encode<<<grid, enc_warps * 32, kEncSmemBytes, s>>>(a, stl);
+        k_scan<uint64_t, true><<<1, 1024, 0, s>>>(a.words_count, g.n_streams, a.stream_off, a.payload_cap, a.status);
+        const uint64_t pack_blocks = (g.n_streams * 32u + 255u) / 256u;
+        k_pack<<<(unsigned)pack_blocks, 256, 0, s>>>(a);
+        k_sizes<<<1, 1, 0, s>>>(a, fixed);
+        CG_CUDA_TRY(cudaGetLastError());
+        CG_CUDA_TRY(cudaMemcpyAsync(&sizes[l], a.dsizes, sizeof(cg_sizes), cudaMemcpyDeviceToHost, s));
+    }
     return CG_OK;
+}
+
+extern "C" cg_status cg_encode(const cg_config *cfg, const uint16_t *kv, void *ws, size_t ws_bytes,
+                               const cg_encoded *out, cg_sizes *sizes, uint32_t *dev_status, void *stream) {
+    const float one = 1.f;
+    return encode_levels(cfg, 1, &one, kv, ws, ws_bytes, out, sizes, dev_status, stream);
+}
+
+extern "C" cg_status cg_encode_levels_ws_bytes(const cg_config *cfg, uint32_t n_levels, size_t *ws_bytes) {
+    Geom g;
+    if (!make_geom(cfg, &g) || !ws_bytes || n_levels == 0 || n_levels > kMaxLevels) return CG_ERR_INVALID_ARG;
+    *ws_bytes = ws_layout(g, n_levels).total;
+    return CG_OK;
+}
+
+extern "C" cg_status cg_encode_levels(const cg_config *cfg, uint32_t n_levels, const float *mult,
+                                      const uint16_t *kv, void *ws, size_t ws_bytes, const cg_encoded *outs,
+                                      cg_sizes *sizes, uint32_t *dev_status, void *stream) {
+    return encode_levels(cfg, n_levels, mult, kv, ws, ws_bytes, outs, sizes, dev_status, stream);
 }

@@ -183,3 +183,21 @@ def test_paged_decode_rejects_bad_layouts_on_host(bt, nb):
     with pytest.raises(C.CodecError) as e:
         C.cg_decode_paged(pc, enc, pool, table, bt, 0, 0, 0, 64, torch.zeros(1, dtype=torch.int32))
     assert e.value.code == C.CG_ERR_INVALID_ARG
+
+
+def test_multi_level_encode_host_checks():
+    pc, _ = P.configs(2, 1000, 64, 10, 0, 128)
+    one = C.cg_encode_levels_ws_bytes(pc, 1)
+    assert one == C.cg_encode_bounds(pc)["workspace_bytes"]
+    assert one < C.cg_encode_levels_ws_bytes(pc, 2) < C.cg_encode_levels_ws_bytes(pc, 4)
+    for bad in (0, 5):
+        with pytest.raises(C.CodecError):
+            C.cg_encode_levels_ws_bytes(pc, bad)
+    # a level whose steps would fall to 2^-10 or below is rejected before any work
+    outs = [C.alloc_encoded(pc, device="cpu") for _ in range(2)]
+    arr = (C.cg_encoded * 2)(*[o.c() for o in outs])
+    sizes = (C.cg_sizes * 2)()
+    mult = np.array([1.0, 1e-4], np.float32)
+    code = C.lib().cg_encode_levels(ct.byref(pc.c()), 2, mult.ctypes.data, 256, 256, 1 << 30, arr,
+                                    ct.addressof(sizes), 0, None)
+    assert code == C.CG_ERR_INVALID_ARG

@@ -345,3 +345,24 @@ def test_paged_decode_block_outside_pool_is_flagged_not_written():
     torch.cuda.synchronize()
     assert C.read_status(status) == C.CG_ERR_RANGE
     assert (pool[npool].cpu().numpy().view(np.uint16) == 0xFFFF).all()
+
+
+@needs_gpu
+@pytest.mark.parametrize("L,T,Cc,chunk,tps,share", [(3, 1100, 64, 256, 100, True), (3, 1100, 64, 256, 100, False),
+                                                    (2, 16384, 1024, 1536, 1536, True)])
+def test_multi_level_encode_matches_oracle_per_level(L, T, Cc, chunk, tps, share):
+    """One cg_encode_levels call (one statistics pass for the x1/x2/x4 levels)
+    gives, level by level, the oracle's object and reconstruction."""
+    x = synth.ar1_kv(L, T, Cc, 0.95, 1, seed=61)
+    x[0, 1, 50, 7] = 20000.0  # escapes at every level
+    x16 = x.numpy().view(np.uint16)
+    pc, _ = P.configs(L, T, Cc, 10, chunk, tps)
+    res = C.encode_levels(pc, x.cuda(), synth.LEVEL_MULTIPLIERS, share_anchors=share)
+    assert len(res) == len(synth.LEVEL_MULTIPLIERS)
+    for (lc, enc), m in zip(res, synth.LEVEL_MULTIPLIERS):
+        _, oc = P.configs(L, T, Cc, 10, chunk, tps, m)
+        assert np.array_equal(lc.step, np.asarray(oc.step, np.float32))
+        oenc = O.encode(oc, x16, nthreads=P.nthreads())
+        P.assert_same_object(P.gpu_to_np(enc), P.oracle_to_np(oenc), f"level x{m}")
+        assert np.array_equal(C.decode(lc, enc).cpu().numpy().view(np.uint16),
+                              O.decode(oc, oenc, nthreads=P.nthreads())), f"level x{m}"
