@@ -355,6 +355,10 @@ def main():
     base = None
     if rank == 0 and not args.no_cpu_baseline:
         base = cpu_baseline(w)
+    # grouping ablation of the same cache (outside the timed region): ideal
+    # bits/value with per-(layer, K/V, channel), per-(layer, K/V) and
+    # whole-cache tables, and with entropy-coded anchors
+    abl = C.ablation(cfg, kv)["bits_per_value"] if rank == 0 else None
 
     if rank == 0:
         line = {
@@ -381,6 +385,7 @@ def main():
             "encode_roofline": {"bound": "hbm", "achieved": round(enc_achieved, 1), "peak": peak, "unit": "GB/s",
                                 "frac": round(enc_achieved / peak, 4)},
             "cpu_baseline": base,
+            "ablation_ideal_bits_per_value": {k: round(v, 4) for k, v in abl.items()},
             "e2e": e2e,
             "gpu_launches": KERNELS_PER_STEP * args.steps,
             "clocks": clk.summary(),

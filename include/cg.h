@@ -307,6 +307,34 @@ cg_status cg_deserialize_header(const void *buf, size_t len, cg_config *cfg, flo
 cg_status cg_deserialize(const void *buf, size_t len, const cg_encoded *obj);
 
 /*
+ * Grouping ablation: ideal coded bits, the sum over symbols of
+ * n_s log2(N / n_s), of the call's delta symbols under three groupings of
+ * the statistics -- one table per (layer, K/V, channel) as the codec does,
+ * one per (layer, K/V), one for the whole cache -- and of the int8 anchors
+ * kept raw (8 bits) or entropy-coded per (layer, K/V, channel).  The
+ * CacheGen pages motivate per-(layer, channel) statistics this way
+ * ("CacheGen vs 传统量化KV缓存压缩技术深度对比与性能测试", §1; sciencestack page,
+ * Figure 5: entropy by grouping strategy).  Escaped values add 32 bits each
+ * in every grouping (escape_bits).  Bits per value of a variant =
+ * (its delta bits + escape_bits + its anchor bits) / values.
+ */
+typedef struct {
+    double values;              /* L * 2 * T * C */
+    double delta_bits_channel;  /* one table per (layer, K/V, channel) */
+    double delta_bits_slice;    /* one table per (layer, K/V) */
+    double delta_bits_global;   /* one table */
+    double escape_bits;         /* 32 per escaped delta */
+    double anchor_bits_raw;     /* 8 per anchor */
+    double anchor_bits_channel; /* anchors entropy-coded per (layer, K/V, channel) */
+} cg_ablation_bits;
+
+/* ws: device, cg_ablation_ws_bytes() bytes, 256-byte aligned; out: device,
+ * valid once the stream has completed; dev_status as for cg_encode. */
+cg_status cg_ablation_ws_bytes(const cg_config *cfg, size_t *ws_bytes);
+cg_status cg_ablation(const cg_config *cfg, const uint16_t *kv, void *ws, size_t ws_bytes, cg_ablation_bits *out,
+                      uint32_t *dev_status, void *stream);
+
+/*
  * Bandwidth-adaptive quality level per chunk (host only).
  * ("CacheGen vs 传统量化KV缓存压缩技术深度对比与性能测试", §2.2: every chunk is
  * stored at several quality levels, and the sender picks a level chunk by

@@ -78,6 +78,10 @@ class cg_paged_kv(ct.Structure):
                 ("kv_stride", ct.c_uint64), ("block_stride", ct.c_uint64), ("token_stride", ct.c_uint64)]
 
 
+ABLATION_FIELDS = ("values", "delta_bits_channel", "delta_bits_slice", "delta_bits_global", "escape_bits",
+                   "anchor_bits_raw", "anchor_bits_channel")
+
+
 class cg_level_plan(ct.Structure):
     _fields_ = [("n_chunks", ct.c_uint32), ("n_levels", ct.c_uint32), ("bytes", ct.c_void_p),
                 ("decode_s", ct.c_void_p), ("bw", ct.c_void_p), ("n_slots", ct.c_uint32), ("slot_s", ct.c_double),
@@ -93,7 +97,7 @@ EXPORTS = ("cg_status_string", "cg_status_from_flags", "cg_encode_bounds", "cg_e
            "cg_decode_chunks_ws_bytes", "cg_decode_chunks", "cg_decode_chunks_noalloc", "cg_chunk_ranges",
            "cg_serialize",
            "cg_deserialize_header", "cg_deserialize", "cg_plan_levels", "cg_decode_paged",
-           "cg_encode_levels_ws_bytes", "cg_encode_levels")
+           "cg_encode_levels_ws_bytes", "cg_encode_levels", "cg_ablation_ws_bytes", "cg_ablation")
 
 _lib = None
 
@@ -121,6 +125,8 @@ def lib() -> ct.CDLL:
         L.cg_deserialize.argtypes = [P, ct.c_size_t, ct.POINTER(cg_encoded)]
         L.cg_plan_levels.argtypes = [ct.POINTER(cg_level_plan), P, P, ct.POINTER(ct.c_double)]
         L.cg_encode_levels_ws_bytes.argtypes = [ct.POINTER(cg_config), U32, ct.POINTER(ct.c_size_t)]
+        L.cg_ablation_ws_bytes.argtypes = [ct.POINTER(cg_config), ct.POINTER(ct.c_size_t)]
+        L.cg_ablation.argtypes = [ct.POINTER(cg_config), P, P, ct.c_size_t, P, P, P]
         L.cg_encode_levels.argtypes = [ct.POINTER(cg_config), U32, P, P, P, ct.c_size_t, P, P, P, P]
         L.cg_decode_paged.argtypes = [ct.POINTER(cg_config), ct.POINTER(cg_encoded), ct.POINTER(cg_paged_kv), P, P]
         for name in EXPORTS:
@@ -511,6 +517,31 @@ def encode_levels(cfg: Config, kv: torch.Tensor, mults: Sequence[float], share_a
                    "n_escapes": int(sz.n_escapes), "total_bytes": int(sz.total_bytes)}
         res.append((c, o.trimmed()))
     return res
+
+
+def ablation(cfg: Config, kv: torch.Tensor, stream=None) -> dict:
+    """Ideal coded bits of the cache's delta symbols with one table per
+    (layer, K/V, channel), per (layer, K/V) or for the whole cache, and of the
+    anchors raw or entropy-coded (cg_ablation); adds bits/value per variant."""
+    dev = kv.device
+    n = ct.c_size_t()
+    _check(lib().cg_ablation_ws_bytes(ct.byref(cfg.c()), ct.byref(n)), "cg_ablation_ws_bytes")
+    ws = torch.empty(n.value, dtype=torch.uint8, device=dev)
+    out = torch.zeros(len(ABLATION_FIELDS), dtype=torch.float64, device=dev)
+    status = new_status(dev)
+    _check(lib().cg_ablation(ct.byref(cfg.c()), kv.data_ptr(), ws.data_ptr(), ws.numel(), out.data_ptr(),
+                             status.data_ptr(), _stream_ptr(stream)), "cg_ablation")
+    torch.cuda.synchronize(dev)
+    _check(read_status(status), "cg_ablation (device)")
+    r = dict(zip(ABLATION_FIELDS, out.cpu().tolist()))
+    v, e = r["values"], r["escape_bits"]
+    r["bits_per_value"] = {
+        "channel_tables": (r["delta_bits_channel"] + e + r["anchor_bits_raw"]) / v,
+        "layer_tables": (r["delta_bits_slice"] + e + r["anchor_bits_raw"]) / v,
+        "one_table": (r["delta_bits_global"] + e + r["anchor_bits_raw"]) / v,
+        "channel_tables_coded_anchors": (r["delta_bits_channel"] + e + r["anchor_bits_channel"]) / v,
+    }
+    return r
 
 
 def decode(cfg: Config, enc: Encoded, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:

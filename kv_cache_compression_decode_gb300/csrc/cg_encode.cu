@@ -17,6 +17,7 @@
 //   k_pack    one warp per stream: copies the stream words into the
 //             payload at its prefix-sum offset, zero-padded to 16 bytes.
 #include <cuda_fp16.h>
+#include <string.h>
 
 #include "cg_internal.cuh"
 
@@ -61,6 +62,9 @@ struct StatsLevels {
     uint16_t *ftab[kMaxLevels];
     uint32_t *tlohi[kMaxLevels], *twidth[kMaxLevels], *esc_count[kMaxLevels];
     float mult[kMaxLevels];
+    // optional raw counts [n_tables][256] of level 0's delta symbols and of
+    // the anchors (q_a + 127), for the grouping ablation; null otherwise
+    uint32_t *raw_delta, *raw_anchor;
 };
 
 // Workspace carving (256-byte aligned pieces): per-level tables and counts,
@@ -149,6 +153,7 @@ __device__ __forceinline__ void stats_full_group(const EncArgs &a, const StatsLe
     nonfinite |= !isfinite(v[0]);
     const float qa = fminf(fmaxf(rintf(__fmul_rn(v[0], inv_sa)), -127.f), 127.f);
     a.anchors[g.anchor_index(slice, c0 + p0) + c] = (int8_t)qa;
+    if (lv.raw_anchor) atomicAdd(&lv.raw_anchor[((uint64_t)slice * g.C + c) * 256u + (uint32_t)((int)qa + 127)], 1u);
     const float xa = __fmul_rn(qa, sa);
 #pragma unroll
     for (uint32_t i = 1; i < N; i++) {
@@ -171,6 +176,7 @@ __device__ __forceinline__ void stats_any_group(const EncArgs &a, const StatsLev
     nonfinite |= !isfinite(v0);
     const float qa = fminf(fmaxf(rintf(__fmul_rn(v0, inv_sa)), -127.f), 127.f);
     a.anchors[g.anchor_index(slice, c0 + p0) + c] = (int8_t)qa;
+    if (lv.raw_anchor) atomicAdd(&lv.raw_anchor[((uint64_t)slice * g.C + c) * 256u + (uint32_t)((int)qa + 127)], 1u);
     const float xa = __fmul_rn(qa, sa);
     for (uint32_t i = 1; i < n; i++) {
         const float vi = ld_half(xp + (uint64_t)i * g.C);
@@ -286,6 +292,9 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 4 : 2) k_stats(Enc
         stats_groups<0, NL>(a, lv, slice, grp, x, sa, inv_sa, inv_step, hist, nonfinite);
     if (__any_sync(kFull, nonfinite) && lane == 0) flag(a.status, CG_ERR_NONFINITE);
     __syncthreads();
+    if (lv.raw_delta)  // level 0's counts, [table][symbol]
+        for (uint32_t i = threadIdx.x; i < 256u * kLanes; i += blockDim.x)
+            lv.raw_delta[((uint64_t)slice * g.C + grp * kLanes + (i & 31u)) * 256u + (i >> 5)] = hist[i];
 
     // E5: normalize each channel's counts to a 16-bit table (warp per
     // (level, channel)).
@@ -712,6 +721,7 @@ static cg_status encode_levels(const cg_config *cfg, uint32_t levels, const floa
         return a;
     };
     StatsLevels lv;
+    lv.raw_delta = lv.raw_anchor = nullptr;
     for (uint32_t l = 0; l < kMaxLevels; l++) {
         const EncArgs a = args(l < levels ? l : 0);
         lv.ftab[l] = a.ftab;
@@ -774,4 +784,169 @@ extern "C" cg_status cg_encode_levels(const cg_config *cfg, uint32_t n_levels, c
                                       const uint16_t *kv, void *ws, size_t ws_bytes, const cg_encoded *outs,
                                       cg_sizes *sizes, uint32_t *dev_status, void *stream) {
     return encode_levels(cfg, n_levels, mult, kv, ws, ws_bytes, outs, sizes, dev_status, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Grouping ablation (the per-(layer, channel) statistics of the CacheGen
+// pages: "CacheGen vs 传统量化KV缓存压缩技术深度对比与性能测试", §1, and the
+// sciencestack page's Figure 5, entropy per grouping strategy).  Ideal coded
+// bits, sum over symbols of n_s log2(N / n_s), of the same delta symbols
+// with one table per (layer, K/V, channel), one per (layer, K/V), or one for
+// the whole cache; and of the int8 anchors kept raw or entropy-coded with
+// one table per (layer, K/V, channel).
+// ---------------------------------------------------------------------------
+namespace cg {
+
+// n log2(N / n) summed over a warp's 8 x 32 bins (counts as doubles).
+__device__ __forceinline__ double warp_bits(const double (&n)[8], double N) {
+    double b = 0.0;
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        if (n[i] > 0.0) b += n[i] * (log2(N) - log2(n[i]));
+    for (int o = 16; o; o >>= 1) b += __shfl_xor_sync(kFull, b, o);
+    return b;
+}
+
+__device__ __forceinline__ double warp_total(const double (&n)[8]) {
+    double t = 0.0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) t += n[i];
+    for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(kFull, t, o);
+    return t;
+}
+
+// Warp per table: bits of each [256] histogram into *bits; 32 bits per
+// count of symbol 255 into *esc when esc is given.
+__global__ void k_bits_tables(const uint32_t *hist, uint64_t n_tables, double *bits, double *esc) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t t = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= n_tables) return;
+    double n[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) n[i] = hist[t * 256u + (uint32_t)i * 32u + lane];
+    const double N = warp_total(n);
+    if (N == 0.0) return;
+    const double b = warp_bits(n, N);
+    if (lane == 0) {
+        atomicAdd(bits, b);
+        if (esc) atomicAdd(esc, 32.0 * (double)hist[t * 256u + 255u]);
+    }
+}
+
+// Block per slice: the slice's C histograms merged into one table; the
+// merged counts are also added to the whole-cache counts.
+__global__ void k_bits_slices(const uint32_t *hist, uint32_t C, double *bits, unsigned long long *global) {
+    __shared__ unsigned long long m[256];
+    const uint64_t t0 = (uint64_t)blockIdx.x * C;
+    for (uint32_t s = threadIdx.x; s < 256u; s += blockDim.x) {
+        unsigned long long v = 0;
+        for (uint32_t c = 0; c < C; c++) v += hist[(t0 + c) * 256u + s];
+        m[s] = v;
+        atomicAdd(&global[s], v);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const uint32_t lane = threadIdx.x;
+        double n[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) n[i] = (double)m[(uint32_t)i * 32u + lane];
+        const double N = warp_total(n);
+        if (N > 0.0) {
+            const double b = warp_bits(n, N);
+            if (lane == 0) atomicAdd(bits, b);
+        }
+    }
+}
+
+__global__ void k_bits_global(const unsigned long long *global, cg_ablation_bits *out, double values,
+                              double anchors) {
+    const uint32_t lane = threadIdx.x;
+    double n[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) n[i] = (double)global[(uint32_t)i * 32u + lane];
+    const double N = warp_total(n);
+    const double b = N > 0.0 ? warp_bits(n, N) : 0.0;
+    if (lane == 0) {
+        out->delta_bits_global = b;
+        out->values = values;
+        out->anchor_bits_raw = 8.0 * anchors;
+    }
+}
+
+struct AblationWs {
+    uint64_t enc, anchors, scales, raw_delta, raw_anchor, global, total;
+};
+static AblationWs ablation_ws(const Geom &g) {
+    AblationWs w;
+    uint64_t o = 0;
+    auto take = [&](uint64_t bytes) {
+        uint64_t at = o;
+        o = round_up(o + bytes, 256);
+        return at;
+    };
+    w.enc = take(ws_layout(g, 1).total);
+    w.anchors = take((uint64_t)g.n_slices * g.A * g.C);
+    w.scales = take(g.n_tables * 4u);
+    w.raw_delta = take(g.n_tables * 256u * 4u);
+    w.raw_anchor = take(g.n_tables * 256u * 4u);
+    w.global = take(256u * 8u);
+    w.total = o;
+    return w;
+}
+
+}  // namespace cg
+
+extern "C" cg_status cg_ablation_ws_bytes(const cg_config *cfg, size_t *ws_bytes) {
+    Geom g;
+    if (!make_geom(cfg, &g) || !ws_bytes) return CG_ERR_INVALID_ARG;
+    *ws_bytes = ablation_ws(g).total;
+    return CG_OK;
+}
+
+extern "C" cg_status cg_ablation(const cg_config *cfg, const uint16_t *kv, void *ws, size_t ws_bytes,
+                                 cg_ablation_bits *out, uint32_t *dev_status, void *stream) {
+    Geom g;
+    if (!make_geom(cfg, &g) || !kv || !ws || !out || reinterpret_cast<uintptr_t>(ws) % 256u) return CG_ERR_INVALID_ARG;
+    const AblationWs W = ablation_ws(g);
+    if (ws_bytes < W.total) return CG_ERR_RANGE;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const WsLayout L = ws_layout(g, 1);
+    uint8_t *we = w + W.enc;
+    EncArgs a;
+    memset(&a, 0, sizeof(a));
+    a.g = g;
+    a.kv = kv;
+    a.anchors = reinterpret_cast<int8_t *>(w + W.anchors);
+    a.scales = reinterpret_cast<float *>(w + W.scales);
+    a.ftab = reinterpret_cast<uint16_t *>(we + L.ftab[0]);
+    a.tlohi = reinterpret_cast<uint32_t *>(we + L.tlohi[0]);
+    a.twidth = reinterpret_cast<uint32_t *>(we + L.twidth[0]);
+    a.esc_count = reinterpret_cast<uint32_t *>(we + L.esc_count[0]);
+    a.status = dev_status;
+    StatsLevels lv;
+    for (uint32_t l = 0; l < kMaxLevels; l++) {
+        lv.ftab[l] = a.ftab;
+        lv.tlohi[l] = a.tlohi;
+        lv.twidth[l] = a.twidth;
+        lv.esc_count[l] = a.esc_count;
+        lv.mult[l] = 1.f;
+    }
+    lv.raw_delta = reinterpret_cast<uint32_t *>(w + W.raw_delta);
+    lv.raw_anchor = reinterpret_cast<uint32_t *>(w + W.raw_anchor);
+    auto *glob = reinterpret_cast<unsigned long long *>(w + W.global);
+    CG_CUDA_TRY(cudaMemsetAsync(a.esc_count, 0, g.n_streams * 4u, s));
+    CG_CUDA_TRY(cudaMemsetAsync(lv.raw_anchor, 0, g.n_tables * 256u * 4u, s));
+    CG_CUDA_TRY(cudaMemsetAsync(glob, 0, 256u * 8u, s));
+    CG_CUDA_TRY(cudaMemsetAsync(out, 0, sizeof(cg_ablation_bits), s));
+    StepTable st;
+    for (uint32_t k = 0; k < g.L; k++) st.v[k] = cfg->step[k];
+    CG_CUDA_TRY(launch_stats<1>(dim3(g.NG, g.n_slices), s, a, st, lv));
+    const unsigned tb = (unsigned)((g.n_tables * 32u + 255u) / 256u);
+    k_bits_tables<<<tb, 256, 0, s>>>(lv.raw_delta, g.n_tables, &out->delta_bits_channel, &out->escape_bits);
+    k_bits_tables<<<tb, 256, 0, s>>>(lv.raw_anchor, g.n_tables, &out->anchor_bits_channel, nullptr);
+    k_bits_slices<<<g.n_slices, 256, 0, s>>>(lv.raw_delta, g.C, &out->delta_bits_slice, glob);
+    k_bits_global<<<1, 32, 0, s>>>(glob, out, (double)g.n_slices * g.T * g.C, (double)g.n_slices * g.A * g.C);
+    CG_CUDA_TRY(cudaGetLastError());
+    return CG_OK;
 }

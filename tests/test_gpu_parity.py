@@ -366,3 +366,43 @@ def test_multi_level_encode_matches_oracle_per_level(L, T, Cc, chunk, tps, share
         P.assert_same_object(P.gpu_to_np(enc), P.oracle_to_np(oenc), f"level x{m}")
         assert np.array_equal(C.decode(lc, enc).cpu().numpy().view(np.uint16),
                               O.decode(oc, oenc, nthreads=P.nthreads())), f"level x{m}"
+
+
+def _bits(counts: np.ndarray) -> float:
+    """Sum over rows of sum_s n_s log2(N / n_s), in float64."""
+    c = counts.astype(np.float64)
+    N = c.sum(axis=-1, keepdims=True)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = np.where(c > 0, c * (np.log2(N) - np.log2(np.where(c > 0, c, 1))), 0.0)
+    return float(t.sum())
+
+
+@needs_gpu
+@pytest.mark.parametrize("L,T,Cc,chunk", [(3, 700, 96, 256), (2, 4096, 1024, 0)])
+def test_grouping_ablation_matches_oracle_counts(L, T, Cc, chunk):
+    """cg_ablation's ideal bits equal the entropies of the oracle's own symbol
+    and anchor counts under the three groupings."""
+    x = synth.ar1_kv(L, T, Cc, 0.9, 2, seed=71)
+    x[1, 0, 33, 5] = 25000.0
+    pc, oc = P.configs(L, T, Cc, 10, chunk, 128)
+    got = C.ablation(pc, x.cuda())
+    xn = x.numpy()
+    sc = O.anchor_scales(oc, xn)
+    anchors, q = O.quantize(oc, xn, sc)
+    h = O.histograms(oc, q).astype(np.int64)  # [L*2*C][256]
+    ah = np.stack([np.bincount(anchors[l, kv, :, c].astype(np.int64) + 127, minlength=256)
+                   for l in range(L) for kv in range(2) for c in range(Cc)])
+    want = {
+        "values": float(L * 2 * T * Cc),
+        "delta_bits_channel": _bits(h),
+        "delta_bits_slice": _bits(h.reshape(L * 2, Cc, 256).sum(axis=1)),
+        "delta_bits_global": _bits(h.sum(axis=0)),
+        "escape_bits": 32.0 * float(h[:, 255].sum()),
+        "anchor_bits_raw": 8.0 * anchors.size,
+        "anchor_bits_channel": _bits(ah),
+    }
+    for k, v in want.items():
+        assert got[k] == pytest.approx(v, rel=1e-12, abs=1e-6), k
+    assert want["escape_bits"] > 0
+    b = got["bits_per_value"]
+    assert b["channel_tables"] < b["layer_tables"] < b["one_table"]
