@@ -3,7 +3,8 @@
 // One thread block per (object, layer, K/V, 32-channel group).  Warp 0 turns
 // the block's 32 compact frequency tables into shared-memory lookup tables,
 // laid out [entry][lane]:
-//   tab    [256][32] u32   c_s | (f_s - 1) << 16
+//   tab    [256][32] u32   c_s | (f_s mod 2^16) << 16 (f = 65536, a single-symbol
+//                          table, is stored as 0 and always takes the full step)
 //   coarse [256][32] u16   bucket b (slots 256 b .. 256 b + 255): s0 << 8 | d,
 //                          s0 the symbol holding slot 256 b, d = 256 (b + 1) -
 //                          (end of s0) when s0 ends inside the bucket, else 0
@@ -80,7 +81,7 @@ constexpr uint32_t kSpinLimit = 1u << 14;               // x 64 us suspend hint:
 static_assert(kLanes * kMaxRun <= (kRingSegs - kAhead - 1) * kSegWords + kSegWords / 4 + 32, "ring window");
 
 // Dynamic shared memory layout of a decode block.
-constexpr uint32_t kTabOff = 0;                              // u32 [256][32]: c | (f-1) << 16
+constexpr uint32_t kTabOff = 0;                              // u32 [256][32]: c | (f mod 2^16) << 16
 constexpr uint32_t kCoarseOff = kTabOff + 256 * kLanes * 4;  // u16 [256][32]: s0 << 8 | d (see top)
 constexpr uint32_t kDqOff = kCoarseOff + 256 * kLanes * 2;   // f32 [256]: float(s - 127) * step
 constexpr uint32_t kHiOff = kDqOff + 256 * 4;                // u32 [32]
@@ -241,18 +242,23 @@ struct Lut {
     uint32_t hi, lane, lt;
 };
 
-// State update for the lane's symbol (r = slot - c_s, fm1 = f_s - 1) and
-// the warp's renormalization: lanes whose state fell below 2^16 take the
-// next words of the stream in lane order.
-__device__ __forceinline__ void update(uint32_t &x, uint32_t &pw, const Lut &T, const uint16_t *ring, uint32_t r,
-                                       uint32_t fm1) {
-    const uint32_t xh = x >> 16;
-    x = xh * fm1 + xh + r;
+// The warp's renormalization of the updated state xn into x: lanes whose
+// state fell below 2^16 take the next words of the stream in lane order.
+__device__ __forceinline__ void renorm(uint32_t &x, uint32_t xn, uint32_t &pw, const Lut &T, const uint16_t *ring) {
+    x = xn;
     const bool need = x < kStateLow;
     const uint32_t bal = __ballot_sync(kFull, need);
     const uint32_t w = ring[(pw + __popc(bal & T.lt)) & (kRingWords - 1u)];
     x = need ? __byte_perm(w, x, 0x5410) : x;  // (x << 16) | w
     pw += __popc(bal);
+}
+
+// State update for the lane's symbol (r = slot - c_s, fm1 = f_s - 1, a
+// form that also holds for f = 65536) and renormalization.
+__device__ __forceinline__ void update(uint32_t &x, uint32_t &pw, const Lut &T, const uint16_t *ring, uint32_t r,
+                                       uint32_t fm1) {
+    const uint32_t xh = x >> 16;
+    renorm(x, xh * fm1 + xh + r, pw, T, ring);
 }
 
 __device__ __forceinline__ uint16_t to_half(float v) { return __half_as_ushort(__float2half_rn(v)); }
@@ -309,6 +315,7 @@ __device__ __forceinline__ bool fast_step(uint32_t &x, uint32_t &pw, const Lut &
     const uint32_t e0 = T.coarse[((x >> 8) & 0xFFu) * kLanes];
     const uint32_t s = (e0 + (x & 0xFFu)) >> 8;
     const uint32_t e = T.tab[s * kLanes];
+    // f = 0 (a single-symbol table) fails r < f and so goes to the full step
     const uint32_t r = (x - e) & 0xFFFFu, fm1 = e >> 16;
     if (__any_sync(kFull, kHasEsc ? (r > fm1 || s == kEsc) : r > fm1)) return false;
     update(x, pw, T, ring, r, fm1);
@@ -320,11 +327,15 @@ __device__ __forceinline__ bool fast_step(uint32_t &x, uint32_t &pw, const Lut &
 // group is token t + k; seek() places t, advance() moves it on.  C is the
 // row length of the [T][C] layout (a compile-time constant where known).
 // [L][2][T][C] layout, shifted by a token offset (chunk destinations).
+template <bool kShift>
 struct LinearOut {
-    uint16_t *base;  // token 0 of the slice, lane's channel
-    int64_t shift;   // destination token = object token + shift
+    uint16_t *base;  // token 0 of the slice
+    int64_t shift;   // destination token = object token + shift (kShift only)
+    uint32_t c;      // lane's channel
     uint16_t *p;
-    __device__ __forceinline__ void seek(uint32_t tok, uint32_t C) { p = base + ((int64_t)tok + shift) * (int64_t)C; }
+    __device__ __forceinline__ void seek(uint32_t tok, uint32_t C) {
+        p = base + ((int64_t)tok + (kShift ? shift : 0)) * (int64_t)C + c;
+    }
     __device__ __forceinline__ uint16_t *row(uint32_t k, uint32_t C) const { return p + (size_t)k * C; }
     __device__ __forceinline__ void advance(uint32_t n, uint32_t C) { p += (size_t)n * C; }
     __device__ __forceinline__ bool ok() const { return true; }
@@ -555,7 +566,7 @@ __global__ void __maxnreg__(kDecRegs) k_decode_all(DecObj o, StepTable st, uint1
             O.good = true;
             alive = decode_span(o, slice, grp, (uint32_t)sp, step, smem, R, O, status);
         } else {
-            const LinearOut O{out + (uint64_t)slice * o.g.T * o.g.C + c, 0, nullptr};
+            const LinearOut<false> O{out + (uint64_t)slice * o.g.T * o.g.C, 0, c, nullptr};
             alive = decode_span(o, slice, grp, (uint32_t)sp, step, smem, R, O, status);
         }
         if (!alive) break;
@@ -577,8 +588,8 @@ __global__ void __maxnreg__(kDecRegs) k_decode_jobs(const DecObj *objs, const De
     for (uint32_t i = warp; i < job.span_count; i += nw) {
         const SpanRef sr = spans[job.span_begin + i];
         const RefDst rd = refs[sr.ref];
-        const LinearOut O{rd.dst + (uint64_t)job.slice * rd.dst_tokens * o.g.C + job.grp * kLanes + (threadIdx.x & 31u),
-                          rd.shift, nullptr};
+        const LinearOut<true> O{rd.dst + (uint64_t)job.slice * rd.dst_tokens * o.g.C, rd.shift,
+                                job.grp * kLanes + (threadIdx.x & 31u), nullptr};
         if (!decode_span(o, job.slice, job.grp, sr.span, step, smem, R, O, status)) break;
     }
 }
