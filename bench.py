@@ -41,7 +41,7 @@ import torch  # noqa: E402
 
 METRIC = "cg_decode / cg_encode GB/s of fp16 KV (1xGB300, % HBM roofline); bits/value"
 UNIT = "GB/s"
-KERNELS_PER_STEP = 8  # k_stats, 3 x k_scan, k_encode, k_pack, k_sizes, k_decode_all
+KERNELS_PER_STEP = 11  # k_stats, 3 x (k_scan_sums + k_scan), k_encode, k_pack, k_sizes, k_decode_all
 # DRAM bytes (read + write) of one k_decode_all launch on the full Llama-70B
 # workload: ncu capture of the first 8 layers (602.7 MB, grows with layers)
 # scaled by 80/8.  Must be reset to None whenever k_decode_all changes.

@@ -9,7 +9,8 @@
 //             histograms (lane = channel, bank = lane: conflict-free
 //             atomics), escape counts per stream, normalization of the 32
 //             histograms to 16-bit frequency tables (warp-cooperative).
-//   k_scan    exclusive scans of table sizes, escape counts and stream sizes.
+//   k_scan    exclusive scans of table sizes, escape counts and stream sizes
+//             (block sums, then each block scans its tile).
 //   k_encode  one warp per stream (lane = channel): interleaved range ANS
 //             over the span's delta tokens in reverse, words written
 //             backwards into a per-stream scratch region, escapes placed
@@ -67,12 +68,15 @@ struct StatsLevels {
     uint32_t *raw_delta, *raw_anchor;
 };
 
+// Prefix scans: kScanThreads threads per block, kScanRows rows each.
+constexpr uint32_t kScanThreads = 256, kScanRows = 16, kScanTile = kScanThreads * kScanRows;
+
 // Workspace carving (256-byte aligned pieces): per-level tables and counts,
 // one scratch region shared by the levels (they are coded one after another).
 struct WsLayout {
     uint64_t ftab[kMaxLevels], tlohi[kMaxLevels], twidth[kMaxLevels], esc_count[kMaxLevels],
         words_count[kMaxLevels], dsizes[kMaxLevels];
-    uint64_t scratch, total, region_words;
+    uint64_t scan_part, scratch, total, region_words;
 };
 
 static WsLayout ws_layout(const Geom &g, uint32_t levels = 1) {
@@ -92,6 +96,8 @@ static WsLayout ws_layout(const Geom &g, uint32_t levels = 1) {
         w.words_count[l] = take(g.n_streams * 4u);
         w.dsizes[l] = take(sizeof(cg_sizes));
     }
+    const uint64_t most = g.n_tables > g.n_streams ? g.n_tables : g.n_streams;
+    w.scan_part = take(((most + kScanTile - 1) / kScanTile + 1) * 8u);
     w.scratch = take(g.n_streams * w.region_words * 2u);
     w.total = o;
     return w;
@@ -386,37 +392,86 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 4 : 2) k_stats(Enc
     }
 }
 
-// Exclusive scan of n u32 values (optionally padded-words -> bytes) into
-// out[0..n] with a single block; flags RANGE if the total exceeds `cap` or
-// the output type.
-template <typename OutT, bool kWordsToBytes>
-__global__ void __launch_bounds__(1024) k_scan(const uint32_t *in, uint64_t n, OutT *out, uint64_t cap,
-                                               uint32_t *status) {
-    __shared__ uint64_t part[1024];
-    const uint32_t tid = threadIdx.x;
-    const uint64_t per = (n + 1023u) / 1024u;
-    const uint64_t b = min((uint64_t)tid * per, n), e = min(b + per, n);
-    auto xf = [](uint32_t v) -> uint64_t { return kWordsToBytes ? round_up(v, 8) * 2u : (uint64_t)v; };
-    uint64_t s = 0;
-    for (uint64_t i = b; i < e; i++) s += xf(in[i]);
-    part[tid] = s;
+// Exclusive scan of n u32 values (optionally padded words -> bytes) into
+// out[0..n], out[n] = total; flags RANGE if the total exceeds `cap` or the
+// output type.  Two passes over tiles of kScanTile values read row by row
+// (coalesced): block sums, then each block scans its tile from the sum of
+// the tiles before it.
+template <bool kWordsToBytes>
+__device__ __forceinline__ uint64_t scan_value(const uint32_t *in, uint64_t i, uint64_t n) {
+    if (i >= n) return 0;
+    const uint32_t v = in[i];
+    return kWordsToBytes ? round_up((uint64_t)v, 8) * 2u : (uint64_t)v;
+}
+
+// Block-wide exclusive scan of one value per thread (kScanThreads threads);
+// *total receives the block's sum.  sh: kScanThreads / 32 words of shared memory.
+__device__ __forceinline__ uint64_t block_exclusive(uint64_t v, uint64_t *total, uint64_t *sh) {
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+    constexpr uint32_t kWarps = kScanThreads / 32;
+    uint64_t x = v;
+    for (uint32_t o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[warp] = x;
     __syncthreads();
-    for (uint32_t o = 1; o < 1024; o <<= 1) {
-        uint64_t v = tid >= o ? part[tid - o] : 0;
-        __syncthreads();
-        part[tid] += v;
-        __syncthreads();
+    if (warp == 0) {
+        uint64_t w = lane < kWarps ? sh[lane] : 0;
+        for (uint32_t o = 1; o < kWarps; o <<= 1) {
+            const uint64_t y = __shfl_up_sync(kFull, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < kWarps) sh[lane] = w;
     }
-    uint64_t run = part[tid] - s;
-    for (uint64_t i = b; i < e; i++) {
-        out[i] = (OutT)run;
-        run += xf(in[i]);
+    __syncthreads();
+    const uint64_t before = warp ? sh[warp - 1] : 0;
+    *total = sh[kWarps - 1];
+    __syncthreads();  // sh is reused by the next call
+    return before + x - v;
+}
+
+template <bool kWordsToBytes>
+__global__ void __launch_bounds__(kScanThreads) k_scan_sums(const uint32_t *in, uint64_t n, uint64_t *part) {
+    __shared__ uint64_t sh[kScanThreads / 32];
+    const uint64_t base = (uint64_t)blockIdx.x * kScanTile;
+    uint64_t v = 0;
+    for (uint32_t r = 0; r < kScanRows; r++) v += scan_value<kWordsToBytes>(in, base + r * kScanThreads + threadIdx.x, n);
+    uint64_t total;
+    block_exclusive(v, &total, sh);
+    if (threadIdx.x == 0) part[blockIdx.x] = total;
+}
+
+template <typename OutT, bool kWordsToBytes>
+__global__ void __launch_bounds__(kScanThreads) k_scan(const uint32_t *in, uint64_t n, const uint64_t *part,
+                                                       OutT *out, uint64_t cap, uint32_t *status) {
+    __shared__ uint64_t sh[kScanThreads / 32];
+    uint64_t pre = 0, total;
+    for (uint32_t b = threadIdx.x; b < blockIdx.x; b += kScanThreads) pre += part[b];
+    block_exclusive(pre, &total, sh);
+    uint64_t run = total;  // sum of the tiles before this one
+    const uint64_t base = (uint64_t)blockIdx.x * kScanTile;
+    for (uint32_t r = 0; r < kScanRows; r++) {
+        const uint64_t i = base + r * kScanThreads + threadIdx.x;
+        const uint64_t v = scan_value<kWordsToBytes>(in, i, n);
+        const uint64_t ex = block_exclusive(v, &total, sh);
+        if (i < n) out[i] = (OutT)(run + ex);
+        run += total;
     }
-    if (tid == 1023) {
-        uint64_t total = part[1023];
-        out[n] = (OutT)total;
-        if (total > cap || total > (uint64_t)(OutT)~(OutT)0) flag(status, CG_ERR_RANGE);
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
+        out[n] = (OutT)run;
+        if (run > cap || run > (uint64_t)(OutT)~(OutT)0) flag(status, CG_ERR_RANGE);
     }
+}
+
+static uint32_t scan_blocks(uint64_t n) { return (uint32_t)((n + kScanTile - 1) / kScanTile) + (n == 0); }
+
+template <typename OutT, bool kWordsToBytes>
+static void launch_scan(const uint32_t *in, uint64_t n, OutT *out, uint64_t cap, uint32_t *status, uint64_t *part,
+                        cudaStream_t s) {
+    const uint32_t nb = scan_blocks(n);
+    k_scan_sums<kWordsToBytes><<<nb, kScanThreads, 0, s>>>(in, n, part);
+    k_scan<OutT, kWordsToBytes><<<nb, kScanThreads, 0, s>>>(in, n, part, out, cap, status);
 }
 
 constexpr int kMaxEncWarps = 12;
@@ -754,10 +809,11 @@ static cg_status encode_levels(const cg_config *cfg, uint32_t levels, const floa
             CG_CUDA_TRY(cudaMemcpyAsync(a.anchors, a0.anchors, bd.anchors_bytes, cudaMemcpyDeviceToDevice, s));
         if (l > 0 && a.scales != a0.scales)
             CG_CUDA_TRY(cudaMemcpyAsync(a.scales, a0.scales, bd.scales_bytes, cudaMemcpyDeviceToDevice, s));
-        k_scan<uint32_t, false><<<1, 1024, 0, s>>>(a.twidth, g.n_tables, a.table_off, a.tables_cap, a.status);
-        k_scan<uint32_t, false><<<1, 1024, 0, s>>>(a.esc_count, g.n_streams, a.esc_off, a.escapes_cap, a.status);
+        uint64_t *part = reinterpret_cast<uint64_t *>(w + L.scan_part);
+        launch_scan<uint32_t, false>(a.twidth, g.n_tables, a.table_off, a.tables_cap, a.status, part, s);
+        launch_scan<uint32_t, false>(a.esc_count, g.n_streams, a.esc_off, a.escapes_cap, a.status, part, s);
         k_encode<<<grid, enc_warps * 32, kEncSmemBytes, s>>>(a, stl);
-        k_scan<uint64_t, true><<<1, 1024, 0, s>>>(a.words_count, g.n_streams, a.stream_off, a.payload_cap, a.status);
+        launch_scan<uint64_t, true>(a.words_count, g.n_streams, a.stream_off, a.payload_cap, a.status, part, s);
         const uint64_t pack_blocks = (g.n_streams * 32u + 255u) / 256u;
         k_pack<<<(unsigned)pack_blocks, 256, 0, s>>>(a);
         k_sizes<<<1, 1, 0, s>>>(a, fixed);
