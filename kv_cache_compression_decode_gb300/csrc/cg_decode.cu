@@ -594,19 +594,18 @@ __global__ void __maxnreg__(kDecRegs) k_decode_jobs(const DecObj *objs, const De
     }
 }
 
+// The kernels' dynamic shared memory limit, set on the current device before
+// each launch (the attribute is per device; setting it is a host-side call).
 static cudaError_t set_smem_attrs() {
-    static cudaError_t err = [] {
-        cudaError_t e = cudaFuncSetAttribute(k_decode_all<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)dec_smem_bytes(kMaxDecWarps));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_decode_all<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)dec_smem_bytes(kMaxDecWarps));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_decode_jobs, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)dec_smem_bytes(kMaxDecWarps));
-        return e;
-    }();
-    return err;
+    cudaError_t e = cudaFuncSetAttribute(k_decode_all<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)dec_smem_bytes(kMaxDecWarps));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_decode_all<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)dec_smem_bytes(kMaxDecWarps));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_decode_jobs, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)dec_smem_bytes(kMaxDecWarps));
+    return e;
 }
 
 static bool fill_obj(const cg_config *cfg, const cg_encoded *enc, DecObj *o) {

@@ -714,8 +714,8 @@ static bool outputs_ok(const cg_encoded *out) {
 template <uint32_t NL>
 static cudaError_t launch_stats(dim3 grid, cudaStream_t s, const EncArgs &a, const StepTable &st, const StatsLevels &lv) {
     constexpr int bytes = (int)(NL * 256u * kLanes * 4u);
-    static const cudaError_t attr =
-        cudaFuncSetAttribute(k_stats<NL>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    // per device, so set before every launch (a host-side call)
+    const cudaError_t attr = cudaFuncSetAttribute(k_stats<NL>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (attr != cudaSuccess) return attr;
     k_stats<NL><<<grid, kStatsWarps * 32, bytes, s>>>(a, st, lv);
     return cudaGetLastError();
@@ -795,9 +795,7 @@ static cg_status encode_levels(const cg_config *cfg, uint32_t levels, const floa
                     : levels == 3 ? launch_stats<3>(grid, s, a0, st, lv)
                                   : launch_stats<4>(grid, s, a0, st, lv);
     CG_CUDA_TRY(e);
-    static const cudaError_t attr =
-        cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEncSmemBytes);
-    CG_CUDA_TRY(attr);
+    CG_CUDA_TRY(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEncSmemBytes));
     const uint32_t enc_warps = (uint32_t)(g.spans_total < (uint64_t)kMaxEncWarps ? g.spans_total : kMaxEncWarps);
     const uint64_t fixed = bd.anchors_bytes + bd.scales_bytes + bd.table_off_bytes + bd.stream_off_bytes +
                            bd.esc_off_bytes;
