@@ -75,10 +75,14 @@ constexpr uint32_t kRingWords = kSegWords * kRingSegs;  // 1024 words = 2 KB per
 constexpr uint32_t kAhead = 4;                          // segments requested ahead of the one awaited
 constexpr uint32_t kMaxRun = 9;                         // steps between ring checks (<= 288 words)
 constexpr uint32_t kSpinLimit = 1u << 14;               // x 64 us suspend hint: ~1 s bound per wait
-// A run of kMaxRun steps reads at most 32 * kMaxRun words past pw; with
-// kRingSegs slots and kAhead segments requested ahead this never overwrites
-// an unread slot (see ensure()).
-static_assert(kLanes * kMaxRun <= (kRingSegs - kAhead - 1) * kSegWords + kSegWords / 4 + 32, "ring window");
+// A run of kMaxRun steps reads words [pw, pw + R), R = 32 * kMaxRun.  The
+// run waits for segment k only when pw + R > k * W (W = kSegWords), and that
+// wait first requests segment k + kAhead into the slot of segment
+// k + kAhead - kRingSegs, whose words end at (k + kAhead - kRingSegs + 1) W.
+// The reads have passed them if pw >= that end, which pw > k W - R gives
+// whenever R <= (kRingSegs - kAhead - 1) W + 1.
+static_assert(kLanes * kMaxRun <= (kRingSegs - kAhead - 1) * kSegWords + 1, "ring window");
+static_assert((kRingSegs & (kRingSegs - 1u)) == 0, "slot = segment & (kRingSegs - 1)");
 
 // Dynamic shared memory layout of a decode block.
 constexpr uint32_t kTabOff = 0;                              // u32 [256][32]: c | (f mod 2^16) << 16
@@ -159,7 +163,7 @@ __device__ __forceinline__ bool ring_wait(Ring &R, uint32_t k) {
 
 // Make words [0, need) of the stream available.  Segment k + kAhead goes
 // into the slot of segment k + kAhead - kRingSegs, which the reads have
-// passed: when segment k is awaited, pw > 128 k - 288 >= 128 (k - 3).
+// passed (the ring-window assertion above).
 __device__ __forceinline__ void ensure(Ring &R, Cursor &K, uint32_t need) {
     while (K.avail < need && K.wseg < K.nseg) {
         __syncwarp();
