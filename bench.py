@@ -159,10 +159,18 @@ def cpu_baseline(workload, seconds_hint=20.0):
             break
     dt = (time.perf_counter() - t0) / reps
     gbs = x16.nbytes / dt / 1e9
+    # one thread on the first layer (two slices), for the per-core figure
+    oc1 = O.Config(1, workload.T, workload.C, 10, workload.chunk, workload.tokens_per_stream,
+                   O.layer_steps(workload.L)[:1])
+    x1 = np.ascontiguousarray(x16[:1])
+    t1 = time.perf_counter()
+    O.decode(oc1, O.encode(oc1, x1, nthreads=1), nthreads=1)
+    gbs1 = x1.nbytes / (time.perf_counter() - t1) / 1e9
     return {"value": gbs, "unit": UNIT, "cores": min(cores, 2 * L1), "kind": "oracle",
+            "single_thread_value": gbs1,
             "sample": f"encode+decode of layers 0..{L1 - 1} ({2 * L1} slices of {workload.T} tokens x "
                       f"{workload.C} channels, {x16.nbytes / 1e6:.0f} MB fp16) of {workload.name}, {reps} reps, "
-                      f"one thread per (layer, K/V) slice"}
+                      f"one thread per (layer, K/V) slice; single_thread_value: layer 0 on one thread"}
 
 
 def run_reference(args):
