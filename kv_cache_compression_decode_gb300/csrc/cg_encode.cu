@@ -502,11 +502,17 @@ struct EncStream {
 // of the state if coding the symbol would overflow it (the warp's emitters
 // write in lane order), then x = floor(x / f) * 2^16 + x mod f + c.
 // etab: [symbol][lane] c | (f - 1) << 16, followed by [symbol][lane] floor((2^32 - 1) / f).
-__device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab, float v, float xa, float inv_step,
-                                         uint32_t lane, uint32_t lt, EncStream &S) {
-    const int q = __float2int_rn(__fmul_rn(__fsub_rn(v, xa), inv_step));
+// q: the lane's quantized delta.  kHasEsc = false when no lane of the warp
+// escapes in this step (the caller checked).
+__device__ __forceinline__ int quantize(float v, float xa, float inv_step) {
+    return __float2int_rn(__fmul_rn(__fsub_rn(v, xa), inv_step));
+}
+
+template <bool kHasEsc>
+__device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab, int q, uint32_t lane, uint32_t lt,
+                                         EncStream &S) {
     const uint32_t s = symbol_of(q);
-    const uint32_t eb = __ballot_sync(kFull, s == kEsc);
+    const uint32_t eb = kHasEsc ? __ballot_sync(kFull, s == kEsc) : 0u;
     if (eb) {
         const uint32_t ne = __popc(eb);
         if (ne > S.e_top) {
@@ -524,10 +530,12 @@ __device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab,
     const bool emit = (S.xs >> 16) >= f;
     const uint32_t mb = __ballot_sync(kFull, emit);
     const uint32_t nem = __popc(mb);
-    if (emit) {
-        S.region[S.top - nem + __popc(mb & lt)] = (uint16_t)(S.xs & 0xFFFFu);
-        S.xs >>= 16;
-    }
+    // branch-free: every lane forms the address, the emitting lanes store
+    uint16_t *dst = S.region + (S.top - nem + __popc(mb & lt));
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.global.u16 [%0], %1;\n\t}"
+                 ::"l"(dst), "h"((unsigned short)(S.xs & 0xFFFFu)), "r"((uint32_t)emit)
+                 : "memory");
+    S.xs = emit ? S.xs >> 16 : S.xs;
     S.top -= nem;
     uint32_t qd, rd;
     udiv_magic(S.xs, f, m, qd, rd);
@@ -576,14 +584,30 @@ __device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *et
         const uint32_t gn = has_next ? gs - G : 0u;
         const bool nxt_full = kG > 1 && has_next && gn >= p0;
         if (nxt_full) load_group(gn, nxt, qa_nxt);
+        // A whole group is quantized first: one vote tells whether any of
+        // its values escapes.  If none does (nearly always), its steps skip
+        // the escape handling; otherwise -- and for groups cut by the span
+        // -- the values are reloaded and coded one by one with it.
+        bool fast = false;
+        int q[kV];
         if (cur_full) {
             const float xa = __fmul_rn(qa_cur, sa);
+            bool esc = false;
 #pragma unroll
-            for (uint32_t i = kV; i-- > 0;) enc_step(a, etab, cur[i], xa, inv_step, lane, lt, S);
+            for (uint32_t i = 0; i < kV; i++) {
+                q[i] = quantize(cur[i], xa, inv_step);
+                esc = esc || symbol_of(q[i]) == kEsc;
+            }
+            fast = !__any_sync(kFull, esc);
+        }
+        if (fast) {
+#pragma unroll
+            for (uint32_t i = kV; i-- > 0;) enc_step<false>(a, etab, q[i], lane, lt, S);
         } else {
             const float xa = __fmul_rn((float)a.anchors[g.anchor_index(slice, c0 + gs) + c], sa);
             const uint32_t t_lo = max(gs + 1u, p0), t_hi = min(gs + G, p1);
-            for (uint32_t t = t_hi; t-- > t_lo;) enc_step(a, etab, ld_half(x + (uint64_t)(c0 + t) * g.C), xa, inv_step, lane, lt, S);
+            for (uint32_t t = t_hi; t-- > t_lo;)
+                enc_step<true>(a, etab, quantize(ld_half(x + (uint64_t)(c0 + t) * g.C), xa, inv_step), lane, lt, S);
         }
         if (!has_next) break;
         gs = gn;
