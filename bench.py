@@ -255,8 +255,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", default="llama70b", choices=["llama70b", "streamed"])
-    ap.add_argument("--stream-tps", type=int, default=768, help="streamed: tokens per stream")
-    ap.add_argument("--stream-cps", type=int, default=6, help="streamed: chunks per pipeline stage")
+    ap.add_argument("--stream-tps", type=int, default=512, help="streamed: tokens per stream")
+    ap.add_argument("--stream-cps", type=int, default=4, help="streamed: chunks per pipeline stage")
     ap.add_argument("--stream-slots", type=int, default=3, help="streamed: staging slots")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: use the first N layers of the workload (not a bench line)")
