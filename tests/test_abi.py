@@ -201,3 +201,19 @@ def test_multi_level_encode_host_checks():
     code = C.lib().cg_encode_levels(ct.byref(pc.c()), 2, mult.ctypes.data, 256, 256, 1 << 30, arr,
                                     ct.addressof(sizes), 0, None)
     assert code == C.CG_ERR_INVALID_ARG
+
+
+def test_ablation_host_checks():
+    """cg_ablation sizes its workspace and rejects bad arguments before any
+    GPU work (no GPU needed)."""
+    pc, _ = P.configs(2, 1000, 64, 10, 0, 128)
+    n = ct.c_size_t()
+    assert C.lib().cg_ablation_ws_bytes(ct.byref(pc.c()), ct.byref(n)) == C.CG_OK
+    assert n.value >= C.cg_encode_bounds(pc)["workspace_bytes"]
+    assert C.lib().cg_ablation_ws_bytes(ct.byref(pc.c()), None) == C.CG_ERR_INVALID_ARG
+    ws = 256
+    # null cache, null output, misaligned workspace, too small a workspace
+    assert C.lib().cg_ablation(ct.byref(pc.c()), None, ws, n.value, 256, 0, None) == C.CG_ERR_INVALID_ARG
+    assert C.lib().cg_ablation(ct.byref(pc.c()), 256, ws, n.value, None, 0, None) == C.CG_ERR_INVALID_ARG
+    assert C.lib().cg_ablation(ct.byref(pc.c()), 256, ws + 8, n.value, 256, 0, None) == C.CG_ERR_INVALID_ARG
+    assert C.lib().cg_ablation(ct.byref(pc.c()), 256, ws, n.value - 1, 256, 0, None) == C.CG_ERR_RANGE
