@@ -116,3 +116,25 @@ def test_planned_levels_drive_the_stream():
         for c, q in enumerate(lv):
             sl = slice(c * chunk, min(T, (c + 1) * chunk))
             assert np.array_equal(got[:, :, sl], odecs_all[j][q][:, :, sl]), f"context {j} chunk {c} level {q}"
+
+
+@needs_gpu
+def test_streamed_full_width_contexts_match_oracle():
+    """Two contexts of the streamed workload at full shape (48 layers x 1024
+    channels, its generator and seeds, 1536-token chunks, 512-token streams),
+    cut to 1-2 chunks, streamed 4 chunks per stage: bit-exact with the oracle."""
+    L, Cc, chunk, tps = synth.STREAM_L, synth.STREAM_C, synth.STREAM_CHUNK, 512
+    ctx, expect = [], []
+    for j, T in enumerate([2000, 1400]):
+        x = synth.stream_context(j, T)
+        pc = C.Config(L, T, Cc, 10, chunk, tps, C.layer_steps(L))
+        oc = O.Config(L, T, Cc, 10, chunk, tps, O.layer_steps(L))
+        enc = C.encode(pc, x.cuda())
+        ctx.append(PL.HostObject.from_device(pc, enc))
+        oenc = O.encode(oc, x.numpy().view(np.uint16), nthreads=P.nthreads())
+        P.assert_same_object(P.gpu_to_np(enc), P.oracle_to_np(oenc), f"context {j}")
+        expect.append(O.decode(oc, oenc, nthreads=P.nthreads()))
+    outs = [torch.empty((L, 2, h.cfg.T, Cc), dtype=torch.float16, device="cuda") for h in ctx]
+    PL.StreamedDecoder(ctx, "cuda", slots=3, chunks_per_stage=4, outputs=outs).run()
+    for j, (o, e) in enumerate(zip(outs, expect)):
+        assert np.array_equal(o.cpu().numpy().view(np.uint16), e), f"context {j}"
