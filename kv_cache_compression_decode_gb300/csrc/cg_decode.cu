@@ -3,8 +3,8 @@
 // One thread block per (object, layer, K/V, 32-channel group).  Warp 0 turns
 // the block's 32 compact frequency tables into shared-memory lookup tables,
 // laid out [entry][lane]:
-//   tab    [256][32] u32   c_s | (f_s mod 2^16) << 16 (f = 65536, a single-symbol
-//                          table, is stored as 0 and always takes the full step)
+//   tab    [256][32] u32   c_s | (f_s - 1) << 16 (f - 1 keeps f = 65536, a
+//                          single-symbol table, within 16 bits)
 //   coarse [256][32] u16   bucket b (slots 256 b .. 256 b + 255): s0 << 8 | d,
 //                          s0 the symbol holding slot 256 b, d = 256 (b + 1) -
 //                          (end of s0) when s0 ends inside the bucket, else 0
@@ -85,7 +85,7 @@ static_assert(kLanes * kMaxRun <= (kRingSegs - kAhead - 1) * kSegWords + 1, "rin
 static_assert((kRingSegs & (kRingSegs - 1u)) == 0, "slot = segment & (kRingSegs - 1)");
 
 // Dynamic shared memory layout of a decode block.
-constexpr uint32_t kTabOff = 0;                              // u32 [256][32]: c | (f mod 2^16) << 16
+constexpr uint32_t kTabOff = 0;                              // u32 [256][32]: c | (f - 1) << 16
 constexpr uint32_t kCoarseOff = kTabOff + 256 * kLanes * 4;  // u16 [256][32]: s0 << 8 | d (see top)
 constexpr uint32_t kDqOff = kCoarseOff + 256 * kLanes * 2;   // f32 [256]: float(s - 127) * step
 constexpr uint32_t kHiOff = kDqOff + 256 * 4;                // u32 [32]
@@ -319,7 +319,6 @@ __device__ __forceinline__ bool fast_step(uint32_t &x, uint32_t &pw, const Lut &
     const uint32_t e0 = T.coarse[((x >> 8) & 0xFFu) * kLanes];
     const uint32_t s = (e0 + (x & 0xFFu)) >> 8;
     const uint32_t e = T.tab[s * kLanes];
-    // f = 0 (a single-symbol table) fails r < f and so goes to the full step
     const uint32_t r = (x - e) & 0xFFFFu, fm1 = e >> 16;
     if (__any_sync(kFull, kHasEsc ? (r > fm1 || s == kEsc) : r > fm1)) return false;
     update(x, pw, T, ring, r, fm1);
