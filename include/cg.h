@@ -136,7 +136,8 @@ cg_status cg_status_from_flags(uint32_t flags);
 cg_status cg_encode_bounds(const cg_config *cfg, cg_bounds *b);
 
 /*
- * Encode kv (device, fp16 bits, [L][2][T][C] contiguous) into `out`.
+ * Encode kv (device, fp16 bits, [L][2][T][C] contiguous, 16-byte aligned:
+ * it is read in 16-byte pieces) into `out`.
  * Implements the whole encoder: anchor scale and int8 anchors, delta
  * quantization with the layer's step (escape symbol 255 for |q| > 127),
  * per-(layer, K/V, channel) histograms normalized to 16-bit frequency tables,
@@ -328,8 +329,9 @@ typedef struct {
     double anchor_bits_channel; /* anchors entropy-coded per (layer, K/V, channel) */
 } cg_ablation_bits;
 
-/* ws: device, cg_ablation_ws_bytes() bytes, 256-byte aligned; out: device,
- * valid once the stream has completed; dev_status as for cg_encode. */
+/* kv as for cg_encode (16-byte aligned); ws: device, cg_ablation_ws_bytes()
+ * bytes, 256-byte aligned; out: device, valid once the stream has completed;
+ * dev_status as for cg_encode. */
 cg_status cg_ablation_ws_bytes(const cg_config *cfg, size_t *ws_bytes);
 cg_status cg_ablation(const cg_config *cfg, const uint16_t *kv, void *ws, size_t ws_bytes, cg_ablation_bits *out,
                       uint32_t *dev_status, void *stream);

@@ -125,7 +125,24 @@ __device__ __forceinline__ void warp_argmax(uint32_t &v, uint32_t &s) {
     }
 }
 
-constexpr int kStatsWarps = 8;
+constexpr int kStatsWarps = 16;
+// Staging of the statistics pass.  A slice's tokens are cut into tiles that
+// never cross a chunk: R rows each, R a whole number of groups when a group
+// fits a slot (such tiles start on an anchor row), else one slot of rows.
+// Every warp takes a contiguous run of tiles and copies them (the block's 32
+// channels: 64 bytes a row) with cp.async into a ring of kStStages
+// shared-memory slots, kStStages - 1 tiles ahead of the one it counts.
+constexpr uint32_t kStSlotRows = 20;
+constexpr uint32_t kStStages = 3;
+constexpr uint32_t kStRowBytes = kLanes * 2u;
+constexpr uint32_t kStSlotBytes = kStSlotRows * kStRowBytes;              // 1280 B
+constexpr uint32_t kStRingBytes = kStatsWarps * kStStages * kStSlotBytes;  // 60 KB
+constexpr uint32_t kE1Batch = 8;  // 16-byte anchor-row loads in flight per lane
+
+template <uint32_t NL>
+constexpr uint32_t stats_smem_bytes() {
+    return NL * 256u * kLanes * 4u + kStRingBytes;
+}
 
 // Token of anchor row r (over all chunks of one slice).
 __device__ __forceinline__ uint32_t anchor_token(const Geom &g, uint32_t r) {
@@ -133,147 +150,184 @@ __device__ __forceinline__ uint32_t anchor_token(const Geom &g, uint32_t r) {
     return ch * g.chunk + (r - ch * g.apc_full) * g.G;
 }
 
-// Quantize one group's anchor and deltas and count the delta symbols.
-// v[0] is the anchor token's value, v[1..N-1] the deltas' (already loaded).
-// Symbol of delta d at each level: count it in that level's histogram
-// (hist + level * 256 * 32) and, for an escape, in the stream's count.
-template <uint32_t NL>
-__device__ __forceinline__ void count_delta(const EncArgs &a, const StatsLevels &lv, float d, const float (&inv_step)[NL],
-                                            uint32_t *hist, uint32_t lane, uint64_t stream) {
-#pragma unroll
-    for (uint32_t l = 0; l < NL; l++) {
-        const int q = __float2int_rn(__fmul_rn(d, inv_step[l]));
-        const uint32_t s = symbol_of(q);
-        atomicAdd(&hist[l * 256u * kLanes + s * kLanes + lane], 1u);
-        if (s == kEsc) atomicAdd(&lv.esc_count[l][stream], 1u);
+__device__ __forceinline__ __half2 u2h2(uint32_t u) {
+    __half2 h;
+    memcpy(&h, &u, 4);
+    return h;
+}
+__device__ __forceinline__ uint32_t h22u(__half2 h) {
+    uint32_t u;
+    memcpy(&u, &h, 4);
+    return u;
+}
+__device__ __forceinline__ float h2f(uint16_t u) { return __half2float(__ushort_as_half(u)); }
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(__cvta_generic_to_global(src))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most kStStages - 1 of this thread's copy groups are pending.
+__device__ __forceinline__ void cp_async_wait_ring() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kStStages - 1u) : "memory");
+}
+
+// Copy rows [t0, t0 + n) (n <= kStSlotRows) of the block's 32 channels into
+// the slot at shared address dst (row k at dst + 64 k): 16-byte pieces, four
+// per row, spread over the lanes.
+__device__ __forceinline__ void stage_tile(uint32_t dst, const uint16_t *xg, uint32_t C, uint32_t t0, uint32_t n,
+                                           uint32_t lane) {
+    for (uint32_t p = lane; p < 4u * n; p += 32u) {
+        const uint32_t row = p >> 2, q = p & 3u;
+        cp_async16(dst + row * kStRowBytes + q * 16u, xg + (uint64_t)(t0 + row) * C + q * 8u);
     }
 }
 
-template <uint32_t N, uint32_t NL>
-__device__ __forceinline__ void stats_full_group(const EncArgs &a, const StatsLevels &lv, uint32_t slice, uint32_t grp,
-                                                 uint32_t ch, uint32_t c0, uint32_t p0, const float (&v)[N], float sa,
-                                                 float inv_sa, const float (&inv_step)[NL], uint32_t *hist,
-                                                 bool &nonfinite) {
-    const Geom &g = a.g;
-    const uint32_t lane = threadIdx.x & 31u, c = grp * kLanes + lane;
-    nonfinite |= !isfinite(v[0]);
-    const float qa = fminf(fmaxf(rintf(__fmul_rn(v[0], inv_sa)), -127.f), 127.f);
-    a.anchors[g.anchor_index(slice, c0 + p0) + c] = (int8_t)qa;
-    if (lv.raw_anchor) atomicAdd(&lv.raw_anchor[((uint64_t)slice * g.C + c) * 256u + (uint32_t)((int)qa + 127)], 1u);
-    const float xa = __fmul_rn(qa, sa);
-#pragma unroll
-    for (uint32_t i = 1; i < N; i++) {
-        nonfinite |= !isfinite(v[i]);
-        count_delta<NL>(a, lv, __fsub_rn(v[i], xa), inv_step, hist, lane,
-                        g.stream_index(ch, slice, (p0 + i) / g.tps, grp));
+// Walk over the tiles of one slice: tile (ch, j) holds the chunk-relative
+// rows [j R, min((j + 1) R, clen)) of chunk ch.
+struct TileCursor {
+    uint32_t ch, j, clen;
+    __device__ __forceinline__ void init(const Geom &g, uint32_t tpc, uint32_t u) {
+        ch = u / tpc;
+        j = u - ch * tpc;
+        clen = g.chunk_len(ch);
     }
-}
-
-// Same for a group of any length n (loads inside the loop).
-template <uint32_t NL>
-__device__ __forceinline__ void stats_any_group(const EncArgs &a, const StatsLevels &lv, uint32_t slice, uint32_t grp,
-                                             uint32_t ch, uint32_t c0, uint32_t p0, uint32_t n, const uint16_t *x,
-                                             float sa, float inv_sa, const float (&inv_step)[NL], uint32_t *hist,
-                                             bool &nonfinite) {
-    const Geom &g = a.g;
-    const uint32_t lane = threadIdx.x & 31u, c = grp * kLanes + lane;
-    const uint16_t *xp = x + (uint64_t)(c0 + p0) * g.C;
-    const float v0 = ld_half(xp);
-    nonfinite |= !isfinite(v0);
-    const float qa = fminf(fmaxf(rintf(__fmul_rn(v0, inv_sa)), -127.f), 127.f);
-    a.anchors[g.anchor_index(slice, c0 + p0) + c] = (int8_t)qa;
-    if (lv.raw_anchor) atomicAdd(&lv.raw_anchor[((uint64_t)slice * g.C + c) * 256u + (uint32_t)((int)qa + 127)], 1u);
-    const float xa = __fmul_rn(qa, sa);
-    for (uint32_t i = 1; i < n; i++) {
-        const float vi = ld_half(xp + (uint64_t)i * g.C);
-        nonfinite |= !isfinite(vi);
-        count_delta<NL>(a, lv, __fsub_rn(vi, xa), inv_step, hist, lane,
-                        g.stream_index(ch, slice, (p0 + i) / g.tps, grp));
-    }
-}
-
-// All groups of one slice and channel group, warps strided over groups.
-// kG > 0: compile-time group size; two whole groups are loaded before either
-// is processed so that 2 kG row loads are in flight per lane.
-template <uint32_t kG, uint32_t NL>
-__device__ __forceinline__ void stats_groups(const EncArgs &a, const StatsLevels &lv, uint32_t slice, uint32_t grp,
-                                             const uint16_t *x, float sa, float inv_sa, const float (&inv_step)[NL],
-                                             uint32_t *hist, bool &nonfinite) {
-    const Geom &g = a.g;
-    const uint32_t warp = threadIdx.x >> 5, A = (uint32_t)g.A;
-    for (uint32_t r0 = warp; r0 < A; r0 += 2u * kStatsWarps) {
-        uint32_t ch[2], c0[2], p0[2], n[2];
-        float v0[kG ? kG : 1], v1[kG ? kG : 1];
-#pragma unroll
-        for (int j = 0; j < 2; j++) {
-            const uint32_t r = r0 + (uint32_t)j * kStatsWarps;
-            n[j] = 0;
-            ch[j] = c0[j] = p0[j] = 0;
-            if (r < A) {
-                ch[j] = r / g.apc_full;
-                c0[j] = ch[j] * g.chunk;
-                p0[j] = (r - ch[j] * g.apc_full) * g.G;
-                n[j] = min(g.G, g.chunk_len(ch[j]) - p0[j]);
-            }
+    __device__ __forceinline__ void next(const Geom &g, uint32_t R) {
+        j++;
+        if (j * R >= clen) {
+            ch++;
+            j = 0;
+            clen = g.chunk_len(ch);
         }
-        if (kG) {
-            if (n[0] == kG) {
-                const uint16_t *xp = x + (uint64_t)(c0[0] + p0[0]) * g.C;
+    }
+    __device__ __forceinline__ uint32_t first(uint32_t R) const { return j * R; }
+    __device__ __forceinline__ uint32_t rows(uint32_t R) const { return min(R, clen - j * R); }
+};
+
+// Symbol of delta d quantized with inverse step inv: q + 127, or the escape
+// symbol for |q| > 127.
+__device__ __forceinline__ uint32_t delta_symbol(float d, float inv) {
+    const int q = __float2int_rn(__fmul_rn(d, inv));
+    return min((uint32_t)q + 127u, kEsc);
+}
+
+// Quantized anchor value of v: clamp(rint(v / s_a), -127, 127).
+__device__ __forceinline__ float anchor_q(float v, float inv_sa) {
+    return fminf(fmaxf(rintf(__fmul_rn(v, inv_sa)), -127.f), 127.f);
+}
+
+// Count m delta rows (row i at rows[i * 32], chunk-relative token pos + i)
+// against anchor value xa at every level; escapes, which are rare, are then
+// counted per stream in a second look at the same rows.
+template <uint32_t NL, uint32_t kM_>
+__device__ __forceinline__ void count_rows(const Geom &g, const StatsLevels &lv, const uint16_t *rows, uint32_t m,
+                                           float xa, const float (&inv_step)[NL], uint32_t *hl, float &nan_acc,
+                                           uint32_t slice, uint32_t grp, uint32_t ch, uint32_t pos) {
+    const uint32_t cnt = kM_ ? kM_ : m;
+    bool esc = false;
+#pragma unroll(kM_ ? kM_ : 3)
+    for (uint32_t i = 0; i < cnt; i++) {
+        const float v = h2f(rows[i * kLanes]);
+        nan_acc = __fmaf_rn(v, 0.f, nan_acc);  // v * 0 is NaN exactly for a NaN or infinite v
+        const float d = __fsub_rn(v, xa);
 #pragma unroll
-                for (uint32_t i = 0; i < (kG ? kG : 1); i++) v0[i] = ld_half(xp + (uint64_t)i * g.C);
-            }
-            if (n[1] == kG) {
-                const uint16_t *xp = x + (uint64_t)(c0[1] + p0[1]) * g.C;
-#pragma unroll
-                for (uint32_t i = 0; i < (kG ? kG : 1); i++) v1[i] = ld_half(xp + (uint64_t)i * g.C);
-            }
+        for (uint32_t l = 0; l < NL; l++) {
+            const uint32_t s = delta_symbol(d, inv_step[l]);
+            atomicAdd(hl + l * 256u * kLanes + s * kLanes, 1u);
+            esc = esc || s == kEsc;
         }
-        if (kG && n[0] == kG)
-            stats_full_group(a, lv, slice, grp, ch[0], c0[0], p0[0], v0, sa, inv_sa, inv_step, hist, nonfinite);
-        else if (n[0])
-            stats_any_group(a, lv, slice, grp, ch[0], c0[0], p0[0], n[0], x, sa, inv_sa, inv_step, hist, nonfinite);
-        if (kG && n[1] == kG)
-            stats_full_group(a, lv, slice, grp, ch[1], c0[1], p0[1], v1, sa, inv_sa, inv_step, hist, nonfinite);
-        else if (n[1])
-            stats_any_group(a, lv, slice, grp, ch[1], c0[1], p0[1], n[1], x, sa, inv_sa, inv_step, hist, nonfinite);
+    }
+    if (__any_sync(kFull, esc)) {
+        for (uint32_t i = 0; i < cnt; i++) {
+            const float d = __fsub_rn(h2f(rows[i * kLanes]), xa);
+#pragma unroll
+            for (uint32_t l = 0; l < NL; l++)
+                if (delta_symbol(d, inv_step[l]) == kEsc)
+                    atomicAdd(&lv.esc_count[l][g.stream_index(ch, slice, (pos + i) / g.tps, grp)], 1u);
+        }
     }
 }
 
 // NL levels in one pass: their histograms side by side in dynamic shared
-// memory (NL x 32 KB); anchors and scales are the same for every level.
-// (Four blocks per SM for one level: the pass waits on memory, so it wants
-// the resident warps; NL > 1 is held to two by its shared memory anyway.)
+// memory (NL x 32 KB), then the warps' staging rings; anchors and scales are
+// the same for every level.
 template <uint32_t NL>
-__global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 4 : 2) k_stats(EncArgs a, StepTable st, StatsLevels lv) {
+__global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(EncArgs a, StepTable st, StatsLevels lv) {
     const Geom &g = a.g;
     const uint32_t grp = blockIdx.x, slice = blockIdx.y;
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
     const uint32_t c = grp * kLanes + lane;
-    const uint16_t *x = a.kv + (uint64_t)slice * g.T * g.C + c;
+    const uint16_t *xg = a.kv + (uint64_t)slice * g.T * g.C + grp * kLanes;  // channel 0 of the group
     const float step = st.v[slice >> 1];
 
-    extern __shared__ __align__(16) uint32_t hist[];  // [level][symbol][lane]
+    extern __shared__ __align__(16) uint32_t hist[];  // [level][symbol][lane], then the rings
     __shared__ float red[kStatsWarps][kLanes];
     __shared__ float s_scale[kLanes];
+    uint8_t *ring = reinterpret_cast<uint8_t *>(hist + NL * 256u * kLanes) + warp * kStStages * kStSlotBytes;
+    const uint32_t ring_s = smem_u32(ring);
+
+    // The warp's run of tiles; its first tiles' copies are in flight during E1.
+    const uint32_t G = g.G;
+    const uint32_t R = G <= kStSlotRows ? G * (kStSlotRows / G) : kStSlotRows;
+    const uint32_t tpc = ceil_div(g.chunk, R);
+    const uint32_t U = (g.n_chunks - 1u) * tpc + ceil_div(g.last_len, R);
+    const uint32_t Uw = ceil_div(U, kStatsWarps);
+    const uint32_t u0 = min(warp * Uw, U), nt = min(U - u0, Uw);
+    TileCursor in, cur;  // next tile to copy, next tile to count
+    in.init(g, tpc, u0);
+    cur = in;
+#pragma unroll
+    for (uint32_t j = 0; j + 1u < kStStages; j++) {
+        if (j < nt) {
+            stage_tile(ring_s + j * kStSlotBytes, xg, g.C, in.ch * g.chunk + in.first(R), in.rows(R), lane);
+            in.next(g, R);
+        }
+        cp_async_commit();
+    }
+    // A run that starts inside a group (groups longer than a slot) needs
+    // that group's anchor value.
+    const uint32_t gpos0 = cur.first(R) % G;
+    const uint16_t a_raw = (nt && gpos0) ? xg[(uint64_t)(cur.ch * g.chunk + cur.first(R) - gpos0) * g.C + lane]
+                                         : (uint16_t)0;
 
     for (uint32_t i = threadIdx.x; i < NL * 256u * kLanes; i += blockDim.x) hist[i] = 0;
 
-    // E1: absmax over this call's anchor rows -> scale = absmax / 127
-    // (four independent row loads in flight per lane).
-    float amax = 0.f;
-    const uint32_t A = (uint32_t)g.A;
-    for (uint32_t r0 = warp; r0 < A; r0 += 4u * kStatsWarps) {
-        float v[4];
+    // E1: absmax over this call's anchor rows -> scale = absmax / 127.  A
+    // lane loads 8 channels (16 bytes) of one row, a warp 8 rows at a time;
+    // |v| and max are exact in fp16.
+    const uint32_t A = (uint32_t)g.A, q = lane & 3u;
+    __half2 m2[4];
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const uint32_t r = r0 + (uint32_t)i * kStatsWarps;
-            v[i] = 0.f;
-            if (r < A) v[i] = ld_half(x + (uint64_t)anchor_token(g, r) * g.C);
+    for (int k = 0; k < 4; k++) m2[k] = __float2half2_rn(0.f);
+    for (uint32_t r0 = warp * 8u + (lane >> 2); r0 < A; r0 += kStatsWarps * 8u * kE1Batch) {
+        uint4 v[kE1Batch];
+#pragma unroll
+        for (uint32_t i = 0; i < kE1Batch; i++) {
+            const uint32_t r = r0 + i * kStatsWarps * 8u;
+            v[i] = r < A ? *reinterpret_cast<const uint4 *>(xg + (uint64_t)anchor_token(g, r) * g.C + q * 8u)
+                         : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int i = 0; i < 4; i++) amax = fmaxf(amax, fabsf(v[i]));
+        for (uint32_t i = 0; i < kE1Batch; i++) {
+            m2[0] = __hmax2(m2[0], __habs2(u2h2(v[i].x)));
+            m2[1] = __hmax2(m2[1], __habs2(u2h2(v[i].y)));
+            m2[2] = __hmax2(m2[2], __habs2(u2h2(v[i].z)));
+            m2[3] = __hmax2(m2[3], __habs2(u2h2(v[i].w)));
+        }
     }
-    red[warp][lane] = amax;
+#pragma unroll
+    for (int k = 0; k < 4; k++)
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) m2[k] = __hmax2(m2[k], u2h2(__shfl_xor_sync(kFull, h22u(m2[k]), o)));
+    if (lane < 4u) {
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            red[warp][q * 8u + 2u * k] = __low2float(m2[k]);
+            red[warp][q * 8u + 2u * k + 1u] = __high2float(m2[k]);
+        }
+    }
     __syncthreads();
     if (warp == 0) {
         float m = red[0][lane];
@@ -285,17 +339,75 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 4 : 2) k_stats(Enc
     __syncthreads();
     const float sa = s_scale[lane];
 
-    // E2 + E3 + E4: one warp per group of tokens (anchor + its deltas); the
-    // 10-token groups of the CacheGen pipeline load two whole groups at once.
-    bool nonfinite = false;
+    // E2 + E3 + E4 over the warp's tiles: an anchor row quantizes and stores
+    // the group's anchor; a delta row counts its symbol at every level.
     const float inv_sa = __fdiv_rn(1.f, sa);  // one rounding each
     float inv_step[NL];
 #pragma unroll
     for (uint32_t l = 0; l < NL; l++) inv_step[l] = __fdiv_rn(1.f, __fmul_rn(step, lv.mult[l]));
-    if (g.G == 10)
-        stats_groups<10, NL>(a, lv, slice, grp, x, sa, inv_sa, inv_step, hist, nonfinite);
-    else
-        stats_groups<0, NL>(a, lv, slice, grp, x, sa, inv_sa, inv_step, hist, nonfinite);
+    uint32_t *hl = hist + lane;
+    uint32_t ach = 0xFFFFFFFFu;  // chunk of the cached anchor base
+    uint64_t abase = 0;          // anchor row of group 0 of chunk ach
+    float xa = gpos0 ? __fmul_rn(anchor_q(h2f(a_raw), inv_sa), sa) : 0.f;
+    float nan_acc = 0.f;
+    for (uint32_t t = 0; t < nt; t++) {
+        if (t + kStStages - 1u < nt) {
+            stage_tile(ring_s + ((t + kStStages - 1u) % kStStages) * kStSlotBytes, xg, g.C,
+                       in.ch * g.chunk + in.first(R), in.rows(R), lane);
+            in.next(g, R);
+        }
+        cp_async_commit();
+        cp_async_wait_ring();
+        __syncwarp();
+        const uint16_t *rows = reinterpret_cast<const uint16_t *>(ring + (t % kStStages) * kStSlotBytes) + lane;
+        const uint32_t ch = cur.ch, p = cur.first(R), n = cur.rows(R);
+        if (ch != ach) {
+            ach = ch;
+            abase = g.chunk_anchor_row0(ch) + (uint64_t)slice * g.apc(ch);
+        }
+        if (G == 10 && n == 20) {  // the common tile: two whole 10-token groups
+#pragma unroll
+            for (uint32_t h = 0; h < 2; h++) {
+                const uint16_t *gr = rows + h * 10u * kLanes;
+                const float v0 = h2f(gr[0]);
+                nan_acc = __fmaf_rn(v0, 0.f, nan_acc);
+                const float qa = anchor_q(v0, inv_sa);
+                a.anchors[(abase + p / 10u + h) * g.C + c] = (int8_t)qa;
+                if (lv.raw_anchor)
+                    atomicAdd(&lv.raw_anchor[((uint64_t)slice * g.C + c) * 256u + (uint32_t)((int)qa + 127)], 1u);
+                xa = __fmul_rn(qa, sa);
+                count_rows<NL, 9>(g, lv, gr + kLanes, 9, xa, inv_step, hl, nan_acc, slice, grp, ch, p + h * 10u + 1u);
+            }
+        } else {  // any group size, a chunk's last tile, or groups cut by tiles
+            uint32_t gi = p / G, gpos = p - gi * G, k = 0;
+            while (k < n) {
+                if (gpos == 0) {  // the group's anchor row
+                    const float v = h2f(rows[k * kLanes]);
+                    nan_acc = __fmaf_rn(v, 0.f, nan_acc);
+                    const float qa = anchor_q(v, inv_sa);
+                    a.anchors[(abase + gi) * g.C + c] = (int8_t)qa;
+                    if (lv.raw_anchor)
+                        atomicAdd(&lv.raw_anchor[((uint64_t)slice * g.C + c) * 256u + (uint32_t)((int)qa + 127)],
+                                  1u);
+                    xa = __fmul_rn(qa, sa);
+                    k++;
+                    gpos = 1;
+                } else {  // the group's delta rows inside this tile (a tile ends with its chunk)
+                    const uint32_t m = min(n - k, G - gpos);
+                    count_rows<NL, 0>(g, lv, rows + k * kLanes, m, xa, inv_step, hl, nan_acc, slice, grp, ch, p + k);
+                    k += m;
+                    gpos += m;
+                }
+                if (gpos == G) {
+                    gpos = 0;
+                    gi++;
+                }
+            }
+        }
+        cur.next(g, R);
+        __syncwarp();  // the slot is read by every lane before it is refilled
+    }
+    const bool nonfinite = nan_acc != nan_acc;
     if (__any_sync(kFull, nonfinite) && lane == 0) flag(a.status, CG_ERR_NONFINITE);
     __syncthreads();
     if (lv.raw_delta)  // level 0's counts, [table][symbol]
@@ -737,7 +849,7 @@ static bool outputs_ok(const cg_encoded *out) {
 
 template <uint32_t NL>
 static cudaError_t launch_stats(dim3 grid, cudaStream_t s, const EncArgs &a, const StepTable &st, const StatsLevels &lv) {
-    constexpr int bytes = (int)(NL * 256u * kLanes * 4u);
+    constexpr int bytes = (int)stats_smem_bytes<NL>();
     // per device, so set before every launch (a host-side call)
     const cudaError_t attr = cudaFuncSetAttribute(k_stats<NL>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (attr != cudaSuccess) return attr;
@@ -756,7 +868,8 @@ static cg_status encode_levels(const cg_config *cfg, uint32_t levels, const floa
                                void *stream) {
     Geom g;
     if (!make_geom(cfg, &g) || levels == 0 || levels > kMaxLevels || !mult) return CG_ERR_INVALID_ARG;
-    if (!kv || !ws || !outs || !sizes || reinterpret_cast<uintptr_t>(ws) % 256u) return CG_ERR_INVALID_ARG;
+    if (!kv || !ws || !outs || !sizes || reinterpret_cast<uintptr_t>(ws) % 256u || reinterpret_cast<uintptr_t>(kv) % 16u)
+        return CG_ERR_INVALID_ARG;
     for (uint32_t l = 0; l < levels; l++) {
         if (!outputs_ok(&outs[l]) || !(mult[l] > 0.f) || !isfinite(mult[l])) return CG_ERR_INVALID_ARG;
         for (uint32_t k = 0; k < g.L; k++) {  // every level's steps must be valid steps
@@ -984,7 +1097,9 @@ extern "C" cg_status cg_ablation_ws_bytes(const cg_config *cfg, size_t *ws_bytes
 extern "C" cg_status cg_ablation(const cg_config *cfg, const uint16_t *kv, void *ws, size_t ws_bytes,
                                  cg_ablation_bits *out, uint32_t *dev_status, void *stream) {
     Geom g;
-    if (!make_geom(cfg, &g) || !kv || !ws || !out || reinterpret_cast<uintptr_t>(ws) % 256u) return CG_ERR_INVALID_ARG;
+    if (!make_geom(cfg, &g) || !kv || !ws || !out || reinterpret_cast<uintptr_t>(ws) % 256u ||
+        reinterpret_cast<uintptr_t>(kv) % 16u)
+        return CG_ERR_INVALID_ARG;
     const AblationWs W = ablation_ws(g);
     if (ws_bytes < W.total) return CG_ERR_RANGE;
     uint8_t *w = static_cast<uint8_t *>(ws);

@@ -201,6 +201,15 @@ def test_multi_level_encode_host_checks():
     code = C.lib().cg_encode_levels(ct.byref(pc.c()), 2, mult.ctypes.data, 256, 256, 1 << 30, arr,
                                     ct.addressof(sizes), 0, None)
     assert code == C.CG_ERR_INVALID_ARG
+    # the cache is read in 16-byte pieces: with every other argument valid,
+    # a cache that is only 2-byte aligned is refused before any CUDA call
+    mult = np.array([1.0, 2.0], np.float32)
+    for kv in (258, 264):
+        code = C.lib().cg_encode_levels(ct.byref(pc.c()), 2, mult.ctypes.data, kv, 256, 1 << 30, arr,
+                                        ct.addressof(sizes), 0, None)
+        assert code == C.CG_ERR_INVALID_ARG
+        code = C.lib().cg_encode(ct.byref(pc.c()), kv, 256, 1 << 30, ct.byref(arr[0]), ct.byref(sizes[0]), 0, None)
+        assert code == C.CG_ERR_INVALID_ARG
 
 
 def test_ablation_host_checks():
@@ -216,4 +225,5 @@ def test_ablation_host_checks():
     assert C.lib().cg_ablation(ct.byref(pc.c()), None, ws, n.value, 256, 0, None) == C.CG_ERR_INVALID_ARG
     assert C.lib().cg_ablation(ct.byref(pc.c()), 256, ws, n.value, None, 0, None) == C.CG_ERR_INVALID_ARG
     assert C.lib().cg_ablation(ct.byref(pc.c()), 256, ws + 8, n.value, 256, 0, None) == C.CG_ERR_INVALID_ARG
+    assert C.lib().cg_ablation(ct.byref(pc.c()), 264, ws, n.value, 256, 0, None) == C.CG_ERR_INVALID_ARG
     assert C.lib().cg_ablation(ct.byref(pc.c()), 256, ws, n.value - 1, 256, 0, None) == C.CG_ERR_RANGE
