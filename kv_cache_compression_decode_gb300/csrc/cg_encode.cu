@@ -175,14 +175,16 @@ __device__ __forceinline__ void cp_async_wait_ring() {
 }
 
 // Copy rows [t0, t0 + n) (n <= kStSlotRows) of the block's 32 channels into
-// the slot at shared address dst (row k at dst + 64 k): 16-byte pieces, four
-// per row, spread over the lanes.
-__device__ __forceinline__ void stage_tile(uint32_t dst, const uint16_t *xg, uint32_t C, uint32_t t0, uint32_t n,
-                                           uint32_t lane) {
-    for (uint32_t p = lane; p < 4u * n; p += 32u) {
-        const uint32_t row = p >> 2, q = p & 3u;
-        cp_async16(dst + row * kStRowBytes + q * 16u, xg + (uint64_t)(t0 + row) * C + q * 8u);
-    }
+// the slot at shared address slot (row k at slot + 64 k) in 16-byte pieces:
+// the lane's pieces are rows lane / 4 + 8 k, quarter lane % 4, so it starts
+// from xl = (row lane / 4, channel 8 (lane % 4)) of the group and C8 = 8 C.
+__device__ __forceinline__ void stage_tile(uint32_t slot, const uint16_t *xl, uint32_t C, uint64_t C8, uint32_t t0,
+                                           uint32_t n, uint32_t lane) {
+    const uint16_t *src = xl + (uint64_t)t0 * C;
+    const uint32_t dst = slot + lane * 16u, r = lane >> 2;
+#pragma unroll
+    for (uint32_t k = 0; k < (kStSlotRows + 7u) / 8u; k++)
+        if (r + 8u * k < n) cp_async16(dst + k * 512u, src + k * C8);
 }
 
 // Walk over the tiles of one slice: tile (ch, j) holds the chunk-relative
@@ -205,6 +207,17 @@ struct TileCursor {
     __device__ __forceinline__ uint32_t first(uint32_t R) const { return j * R; }
     __device__ __forceinline__ uint32_t rows(uint32_t R) const { return min(R, clen - j * R); }
 };
+
+// floor(n * 65536 / N) for n <= N, exactly: a float estimate (within one of
+// the quotient, which is at most 65536, for rN = 1/N rounded) corrected by
+// the integer remainder.
+__device__ __forceinline__ uint32_t scaled_count(uint32_t n, uint32_t N, float rN) {
+    uint32_t q = __float2uint_rz(__fmul_rn(__fmul_rn(__uint2float_rn(n), rN), 65536.f));
+    const int64_t r = (int64_t)((uint64_t)n << 16) - (int64_t)((uint64_t)q * N);
+    if (r < 0) q--;
+    else if (r >= (int64_t)N) q++;
+    return q;
+}
 
 // Symbol of delta d quantized with inverse step inv: q + 127, or the escape
 // symbol for |q| > 127.
@@ -275,13 +288,15 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
     const uint32_t U = (g.n_chunks - 1u) * tpc + ceil_div(g.last_len, R);
     const uint32_t Uw = ceil_div(U, kStatsWarps);
     const uint32_t u0 = min(warp * Uw, U), nt = min(U - u0, Uw);
+    const uint16_t *xl = xg + (uint64_t)(lane >> 2) * g.C + (lane & 3u) * 8u;
+    const uint64_t C8 = 8ull * g.C;
     TileCursor in, cur;  // next tile to copy, next tile to count
     in.init(g, tpc, u0);
     cur = in;
 #pragma unroll
     for (uint32_t j = 0; j + 1u < kStStages; j++) {
         if (j < nt) {
-            stage_tile(ring_s + j * kStSlotBytes, xg, g.C, in.ch * g.chunk + in.first(R), in.rows(R), lane);
+            stage_tile(ring_s + j * kStSlotBytes, xl, g.C, C8, in.ch * g.chunk + in.first(R), in.rows(R), lane);
             in.next(g, R);
         }
         cp_async_commit();
@@ -352,7 +367,7 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
     float nan_acc = 0.f;
     for (uint32_t t = 0; t < nt; t++) {
         if (t + kStStages - 1u < nt) {
-            stage_tile(ring_s + ((t + kStStages - 1u) % kStStages) * kStSlotBytes, xg, g.C,
+            stage_tile(ring_s + ((t + kStStages - 1u) % kStStages) * kStSlotBytes, xl, g.C, C8,
                        in.ch * g.chunk + in.first(R), in.rows(R), lane);
             in.next(g, R);
         }
@@ -437,6 +452,7 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
             }
         }
         N = warp_sum(N);
+        const float rN = __frcp_rn(__uint2float_rn(N));  // used only when N > 0
         for (int o = 16; o; o >>= 1) {
             lo = min(lo, __shfl_xor_sync(kFull, lo, o));
             hi = max(hi, __shfl_xor_sync(kFull, hi, o));
@@ -455,8 +471,8 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
             uint32_t s = (uint32_t)i * 32u + lane;
             f[i] = 0;
             if (s >= lo && s <= hi) {
-                uint64_t v = ((uint64_t)n[i] * kM) / N;
-                f[i] = v < 1u ? 1u : (uint32_t)v;
+                const uint32_t v = scaled_count(n[i], N, rN);
+                f[i] = v < 1u ? 1u : v;
             }
             sum += f[i];
             if (n[i] > bn) {
