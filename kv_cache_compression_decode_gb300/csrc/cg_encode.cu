@@ -672,14 +672,17 @@ __device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab,
 
 // Encode one stream: groups from the span's last to its first, each group's
 // deltas in reverse.  Whole groups (kG deltas + anchor inside the span) are
-// loaded one group ahead of the one being coded.
-template <uint32_t kG>
+// loaded one group ahead of the one being coded.  kC = 1024 fixes the row
+// stride at compile time (0: runtime); the group's rows and its anchor are
+// reached by pointers stepped back one group at a time.
+template <uint32_t kG, uint32_t kC>
 __device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *etab, const uint16_t *x, uint32_t slice,
                                             uint32_t grp, uint32_t ch, uint32_t span, float sa, float inv_step) {
     const Geom &g = a.g;
     const uint32_t lane = threadIdx.x & 31u, lt = lanemask_lt();
     const uint32_t c = grp * kLanes + lane;
     const uint32_t G = kG ? kG : g.G;
+    const uint32_t C = kC ? kC : g.C;
     constexpr uint32_t kV = kG > 1 ? kG - 1u : 1u;
     const uint32_t c0 = ch * g.chunk, len = g.chunk_len(ch);
     const uint32_t p0 = span * g.tps, p1 = min(p0 + g.tps, len);
@@ -697,21 +700,23 @@ __device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *et
     S.xs = kStateLow;
 
     uint32_t gs = (p1 - 1u) - (p1 - 1u) % G;  // chunk position of the last group's anchor
+    // this group's anchor (row gs / G of the chunk's anchor rows of this slice) and first row
+    const int8_t *ap = a.anchors + (g.chunk_anchor_row0(ch) + (uint64_t)slice * g.apc(ch) + gs / G) * C + c;
+    const uint16_t *xp = x + (uint64_t)(c0 + gs) * C;
     float cur[kV], nxt[kV];
     float qa_cur = 0.f, qa_nxt = 0.f;
-    auto load_group = [&](uint32_t gpos, float (&buf)[kV], float &qa) {
-        const uint16_t *xp = x + (uint64_t)(c0 + gpos + 1u) * g.C;
+    auto load_group = [&](const uint16_t *gp, const int8_t *gap, float (&buf)[kV], float &qa) {
 #pragma unroll
-        for (uint32_t i = 0; i < kV; i++) buf[i] = ld_half(xp + (uint64_t)i * g.C);
-        qa = (float)a.anchors[g.anchor_index(slice, c0 + gpos) + c];
+        for (uint32_t i = 0; i < kV; i++) buf[i] = ld_half(gp + (uint64_t)(i + 1u) * C);
+        qa = (float)*gap;
     };
     bool cur_full = kG > 1 && gs >= p0 && gs + G <= p1;
-    if (cur_full) load_group(gs, cur, qa_cur);
+    if (cur_full) load_group(xp, ap, cur, qa_cur);
     while (true) {
         const bool has_next = gs > p0;
         const uint32_t gn = has_next ? gs - G : 0u;
         const bool nxt_full = kG > 1 && has_next && gn >= p0;
-        if (nxt_full) load_group(gn, nxt, qa_nxt);
+        if (nxt_full) load_group(xp - (uint64_t)G * C, ap - C, nxt, qa_nxt);
         // A whole group is quantized first: one vote tells whether any of
         // its values escapes.  If none does (nearly always), its steps skip
         // the escape handling; otherwise -- and for groups cut by the span
@@ -732,13 +737,15 @@ __device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *et
 #pragma unroll
             for (uint32_t i = kV; i-- > 0;) enc_step<false>(a, etab, q[i], lane, lt, S);
         } else {
-            const float xa = __fmul_rn((float)a.anchors[g.anchor_index(slice, c0 + gs) + c], sa);
+            const float xa = __fmul_rn((float)*ap, sa);
             const uint32_t t_lo = max(gs + 1u, p0), t_hi = min(gs + G, p1);
             for (uint32_t t = t_hi; t-- > t_lo;)
-                enc_step<true>(a, etab, quantize(ld_half(x + (uint64_t)(c0 + t) * g.C), xa, inv_step), lane, lt, S);
+                enc_step<true>(a, etab, quantize(ld_half(xp + (uint64_t)(t - gs) * C), xa, inv_step), lane, lt, S);
         }
         if (!has_next) break;
         gs = gn;
+        xp -= (uint64_t)G * C;
+        ap -= C;
         cur_full = nxt_full;
         qa_cur = qa_nxt;
 #pragma unroll
@@ -754,7 +761,9 @@ __device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *et
 }
 
 // One block per (32-channel group, slice); one warp per stream of that
-// column (up to kMaxEncWarps, then warps take several).
+// column (up to kMaxEncWarps, then warps take several).  kG / kC: the
+// compile-time group size and row stride of encode_span (0: runtime).
+template <uint32_t kG, uint32_t kC>
 __global__ void __launch_bounds__(kMaxEncWarps * 32, 3) k_encode(EncArgs a, StepTable st) {
     const Geom &g = a.g;
     const uint32_t grp = blockIdx.x, slice = blockIdx.y;
@@ -794,10 +803,7 @@ __global__ void __launch_bounds__(kMaxEncWarps * 32, 3) k_encode(EncArgs a, Step
 
     for (uint64_t sp = warp; sp < g.spans_total; sp += nwarps) {
         const uint32_t ch = (uint32_t)(sp / g.spans_full), span = (uint32_t)(sp - (uint64_t)ch * g.spans_full);
-        if (g.G == 10)
-            encode_span<10>(a, etab, x, slice, grp, ch, span, sa, inv_step);
-        else
-            encode_span<0>(a, etab, x, slice, grp, ch, span, sa, inv_step);
+        encode_span<kG, kC>(a, etab, x, slice, grp, ch, span, sa, inv_step);
     }
 }
 
@@ -948,7 +954,8 @@ static cg_status encode_levels(const cg_config *cfg, uint32_t levels, const floa
                     : levels == 3 ? launch_stats<3>(grid, s, a0, st, lv)
                                   : launch_stats<4>(grid, s, a0, st, lv);
     CG_CUDA_TRY(e);
-    CG_CUDA_TRY(cudaFuncSetAttribute(k_encode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEncSmemBytes));
+    auto k_enc = g.G == 10 && g.C == 1024 ? k_encode<10, 1024> : g.G == 10 ? k_encode<10, 0> : k_encode<0, 0>;
+    CG_CUDA_TRY(cudaFuncSetAttribute(k_enc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEncSmemBytes));
     const uint32_t enc_warps = (uint32_t)(g.spans_total < (uint64_t)kMaxEncWarps ? g.spans_total : kMaxEncWarps);
     const uint64_t fixed = bd.anchors_bytes + bd.scales_bytes + bd.table_off_bytes + bd.stream_off_bytes +
                            bd.esc_off_bytes;
@@ -963,7 +970,7 @@ static cg_status encode_levels(const cg_config *cfg, uint32_t levels, const floa
         uint64_t *part = reinterpret_cast<uint64_t *>(w + L.scan_part);
         launch_scan<uint32_t, false>(a.twidth, g.n_tables, a.table_off, a.tables_cap, a.status, part, s);
         launch_scan<uint32_t, false>(a.esc_count, g.n_streams, a.esc_off, a.escapes_cap, a.status, part, s);
-        k_encode<<<grid, enc_warps * 32, kEncSmemBytes, s>>>(a, stl);
+        k_enc<<<grid, enc_warps * 32, kEncSmemBytes, s>>>(a, stl);
         launch_scan<uint64_t, true>(a.words_count, g.n_streams, a.stream_off, a.payload_cap, a.status, part, s);
         const uint64_t pack_blocks = (g.n_streams * 32u + 255u) / 256u;
         k_pack<<<(unsigned)pack_blocks, 256, 0, s>>>(a);
