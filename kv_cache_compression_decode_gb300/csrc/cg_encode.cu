@@ -47,6 +47,7 @@ struct EncArgs {
     uint32_t *esc_count;   // [n_streams]
     uint32_t *words_count; // [n_streams]
     uint16_t *scratch;     // [n_streams][region_words]
+    const uint8_t *sym;    // [slice][T][C] delta symbols of this level (written by the statistics pass)
     uint64_t region_words;
     cg_sizes *dsizes;
     uint32_t *status;
@@ -66,6 +67,10 @@ struct StatsLevels {
     // optional raw counts [n_tables][256] of level 0's delta symbols and of
     // the anchors (q_a + 127), for the grouping ablation; null otherwise
     uint32_t *raw_delta, *raw_anchor;
+    // every delta's symbol, [level][slice][T][C] (level l at sym + l * sym_stride;
+    // anchor rows are not written), so that the coder does not quantize again
+    uint8_t *sym;
+    uint64_t sym_stride;
 };
 
 // Prefix scans: kScanThreads threads per block, kScanRows rows each.
@@ -76,7 +81,7 @@ constexpr uint32_t kScanThreads = 256, kScanRows = 16, kScanTile = kScanThreads 
 struct WsLayout {
     uint64_t ftab[kMaxLevels], tlohi[kMaxLevels], twidth[kMaxLevels], esc_count[kMaxLevels],
         words_count[kMaxLevels], dsizes[kMaxLevels];
-    uint64_t scan_part, scratch, total, region_words;
+    uint64_t scan_part, scratch, sym, sym_stride, total, region_words;
 };
 
 static WsLayout ws_layout(const Geom &g, uint32_t levels = 1) {
@@ -99,6 +104,8 @@ static WsLayout ws_layout(const Geom &g, uint32_t levels = 1) {
     const uint64_t most = g.n_tables > g.n_streams ? g.n_tables : g.n_streams;
     w.scan_part = take(((most + kScanTile - 1) / kScanTile + 1) * 8u);
     w.scratch = take(g.n_streams * w.region_words * 2u);
+    w.sym_stride = round_up((uint64_t)g.n_slices * g.T * g.C, 256);
+    w.sym = take(w.sym_stride * levels);
     w.total = o;
     return w;
 }
@@ -232,13 +239,15 @@ __device__ __forceinline__ float anchor_q(float v, float inv_sa) {
 }
 
 // Count m delta rows (row i at rows[i * 32], chunk-relative token pos + i)
-// against anchor value xa at every level; escapes, which are rare, are then
+// against anchor value xa at every level and store their symbols (row i of
+// level l at sp + l * sym_stride + i * C); escapes, which are rare, are then
 // counted per stream in a second look at the same rows.
-template <uint32_t NL, uint32_t kM_>
+template <uint32_t NL, uint32_t kM_, uint32_t kC>
 __device__ __forceinline__ void count_rows(const Geom &g, const StatsLevels &lv, const uint16_t *rows, uint32_t m,
-                                           float xa, const float (&inv_step)[NL], uint32_t *hl, float &nan_acc,
-                                           uint32_t slice, uint32_t grp, uint32_t ch, uint32_t pos) {
+                                           float xa, const float (&inv_step)[NL], uint32_t *hl, uint8_t *sp,
+                                           float &nan_acc, uint32_t slice, uint32_t grp, uint32_t ch, uint32_t pos) {
     const uint32_t cnt = kM_ ? kM_ : m;
+    const uint32_t C = kC ? kC : g.C;
     bool esc = false;
 #pragma unroll(kM_ ? kM_ : 3)
     for (uint32_t i = 0; i < cnt; i++) {
@@ -249,6 +258,7 @@ __device__ __forceinline__ void count_rows(const Geom &g, const StatsLevels &lv,
         for (uint32_t l = 0; l < NL; l++) {
             const uint32_t s = delta_symbol(d, inv_step[l]);
             atomicAdd(hl + l * 256u * kLanes + s * kLanes, 1u);
+            sp[l * lv.sym_stride + (uint64_t)i * C] = (uint8_t)s;
             esc = esc || s == kEsc;
         }
     }
@@ -265,8 +275,9 @@ __device__ __forceinline__ void count_rows(const Geom &g, const StatsLevels &lv,
 
 // NL levels in one pass: their histograms side by side in dynamic shared
 // memory (NL x 32 KB), then the warps' staging rings; anchors and scales are
-// the same for every level.
-template <uint32_t NL>
+// the same for every level.  kC = 1024 fixes the row stride of the symbol
+// stores at compile time (0: runtime).
+template <uint32_t NL, uint32_t kC>
 __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(EncArgs a, StepTable st, StatsLevels lv) {
     const Geom &g = a.g;
     const uint32_t grp = blockIdx.x, slice = blockIdx.y;
@@ -376,6 +387,7 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
         __syncwarp();
         const uint16_t *rows = reinterpret_cast<const uint16_t *>(ring + (t % kStStages) * kStSlotBytes) + lane;
         const uint32_t ch = cur.ch, p = cur.first(R), n = cur.rows(R);
+        uint8_t *spt = lv.sym + ((uint64_t)slice * g.T + ch * g.chunk + p) * (kC ? kC : g.C) + c;  // row 0 of the tile
         if (ch != ach) {
             ach = ch;
             abase = g.chunk_anchor_row0(ch) + (uint64_t)slice * g.apc(ch);
@@ -391,7 +403,8 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
                 if (lv.raw_anchor)
                     atomicAdd(&lv.raw_anchor[((uint64_t)slice * g.C + c) * 256u + (uint32_t)((int)qa + 127)], 1u);
                 xa = __fmul_rn(qa, sa);
-                count_rows<NL, 9>(g, lv, gr + kLanes, 9, xa, inv_step, hl, nan_acc, slice, grp, ch, p + h * 10u + 1u);
+                count_rows<NL, 9, kC>(g, lv, gr + kLanes, 9, xa, inv_step, hl, spt + (h * 10u + 1u) * (kC ? kC : g.C),
+                                      nan_acc, slice, grp, ch, p + h * 10u + 1u);
             }
         } else {  // any group size, a chunk's last tile, or groups cut by tiles
             uint32_t gi = p / G, gpos = p - gi * G, k = 0;
@@ -409,7 +422,8 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
                     gpos = 1;
                 } else {  // the group's delta rows inside this tile (a tile ends with its chunk)
                     const uint32_t m = min(n - k, G - gpos);
-                    count_rows<NL, 0>(g, lv, rows + k * kLanes, m, xa, inv_step, hl, nan_acc, slice, grp, ch, p + k);
+                    count_rows<NL, 0, kC>(g, lv, rows + k * kLanes, m, xa, inv_step, hl,
+                                          spt + (uint64_t)k * (kC ? kC : g.C), nan_acc, slice, grp, ch, p + k);
                     k += m;
                     gpos += m;
                 }
@@ -630,16 +644,16 @@ struct EncStream {
 // of the state if coding the symbol would overflow it (the warp's emitters
 // write in lane order), then x = floor(x / f) * 2^16 + x mod f + c.
 // etab: [symbol][lane] c | (f - 1) << 16, followed by [symbol][lane] floor((2^32 - 1) / f).
-// q: the lane's quantized delta.  kHasEsc = false when no lane of the warp
-// escapes in this step (the caller checked).
+// s: the lane's symbol, q: its quantized delta (read only for an escape).
+// kHasEsc = false when no lane of the warp escapes in this step (the caller
+// checked).
 __device__ __forceinline__ int quantize(float v, float xa, float inv_step) {
     return __float2int_rn(__fmul_rn(__fsub_rn(v, xa), inv_step));
 }
 
 template <bool kHasEsc>
-__device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab, int q, uint32_t lane, uint32_t lt,
-                                         EncStream &S) {
-    const uint32_t s = symbol_of(q);
+__device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab, uint32_t s, int q, uint32_t lane,
+                                         uint32_t lt, EncStream &S) {
     const uint32_t eb = kHasEsc ? __ballot_sync(kFull, s == kEsc) : 0u;
     if (eb) {
         const uint32_t ne = __popc(eb);
@@ -671,10 +685,11 @@ __device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab,
 }
 
 // Encode one stream: groups from the span's last to its first, each group's
-// deltas in reverse.  Whole groups (kG deltas + anchor inside the span) are
-// loaded one group ahead of the one being coded.  kC = 1024 fixes the row
-// stride at compile time (0: runtime); the group's rows and its anchor are
-// reached by pointers stepped back one group at a time.
+// deltas in reverse.  The symbols of whole groups (kG deltas + anchor inside
+// the span), as the statistics pass stored them, are loaded one group ahead
+// of the one being coded.  kC = 1024 fixes the row stride at compile time (0:
+// runtime); the group's rows and its anchor are reached by pointers stepped
+// back one group at a time.
 template <uint32_t kG, uint32_t kC>
 __device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *etab, const uint16_t *x, uint32_t slice,
                                             uint32_t grp, uint32_t ch, uint32_t span, float sa, float inv_step) {
@@ -703,51 +718,47 @@ __device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *et
     // this group's anchor (row gs / G of the chunk's anchor rows of this slice) and first row
     const int8_t *ap = a.anchors + (g.chunk_anchor_row0(ch) + (uint64_t)slice * g.apc(ch) + gs / G) * C + c;
     const uint16_t *xp = x + (uint64_t)(c0 + gs) * C;
-    float cur[kV], nxt[kV];
-    float qa_cur = 0.f, qa_nxt = 0.f;
-    auto load_group = [&](const uint16_t *gp, const int8_t *gap, float (&buf)[kV], float &qa) {
+    const uint8_t *sp = a.sym + ((uint64_t)slice * g.T + c0 + gs) * C + c;
+    uint32_t cur[kV], nxt[kV];
+    auto load_group = [&](const uint8_t *gp, uint32_t (&buf)[kV]) {
 #pragma unroll
-        for (uint32_t i = 0; i < kV; i++) buf[i] = ld_half(gp + (uint64_t)(i + 1u) * C);
-        qa = (float)*gap;
+        for (uint32_t i = 0; i < kV; i++) buf[i] = gp[(uint64_t)(i + 1u) * C];
     };
     bool cur_full = kG > 1 && gs >= p0 && gs + G <= p1;
-    if (cur_full) load_group(xp, ap, cur, qa_cur);
+    if (cur_full) load_group(sp, cur);
     while (true) {
         const bool has_next = gs > p0;
         const uint32_t gn = has_next ? gs - G : 0u;
         const bool nxt_full = kG > 1 && has_next && gn >= p0;
-        if (nxt_full) load_group(xp - (uint64_t)G * C, ap - C, nxt, qa_nxt);
-        // A whole group is quantized first: one vote tells whether any of
-        // its values escapes.  If none does (nearly always), its steps skip
-        // the escape handling; otherwise -- and for groups cut by the span
-        // -- the values are reloaded and coded one by one with it.
+        if (nxt_full) load_group(sp - (uint64_t)G * C, nxt);
+        // One vote per whole group tells whether any of its values escapes.
+        // If none does (nearly always), its steps skip the escape handling;
+        // otherwise -- and for groups cut by the span -- the values are
+        // reloaded, quantized and coded one by one with it.
         bool fast = false;
-        int q[kV];
         if (cur_full) {
-            const float xa = __fmul_rn(qa_cur, sa);
             bool esc = false;
 #pragma unroll
-            for (uint32_t i = 0; i < kV; i++) {
-                q[i] = quantize(cur[i], xa, inv_step);
-                esc = esc || symbol_of(q[i]) == kEsc;
-            }
+            for (uint32_t i = 0; i < kV; i++) esc = esc || cur[i] == kEsc;
             fast = !__any_sync(kFull, esc);
         }
         if (fast) {
 #pragma unroll
-            for (uint32_t i = kV; i-- > 0;) enc_step<false>(a, etab, q[i], lane, lt, S);
+            for (uint32_t i = kV; i-- > 0;) enc_step<false>(a, etab, cur[i], 0, lane, lt, S);
         } else {
             const float xa = __fmul_rn((float)*ap, sa);
             const uint32_t t_lo = max(gs + 1u, p0), t_hi = min(gs + G, p1);
-            for (uint32_t t = t_hi; t-- > t_lo;)
-                enc_step<true>(a, etab, quantize(ld_half(xp + (uint64_t)(t - gs) * C), xa, inv_step), lane, lt, S);
+            for (uint32_t t = t_hi; t-- > t_lo;) {
+                const int q = quantize(ld_half(xp + (uint64_t)(t - gs) * C), xa, inv_step);
+                enc_step<true>(a, etab, symbol_of(q), q, lane, lt, S);
+            }
         }
         if (!has_next) break;
         gs = gn;
         xp -= (uint64_t)G * C;
+        sp -= (uint64_t)G * C;
         ap -= C;
         cur_full = nxt_full;
-        qa_cur = qa_nxt;
 #pragma unroll
         for (uint32_t i = 0; i < kV; i++) cur[i] = nxt[i];
     }
@@ -872,10 +883,11 @@ static bool outputs_ok(const cg_encoded *out) {
 template <uint32_t NL>
 static cudaError_t launch_stats(dim3 grid, cudaStream_t s, const EncArgs &a, const StepTable &st, const StatsLevels &lv) {
     constexpr int bytes = (int)stats_smem_bytes<NL>();
+    auto k = NL == 1 && a.g.C == 1024 ? k_stats<NL, (NL == 1 ? 1024u : 0u)> : k_stats<NL, 0>;
     // per device, so set before every launch (a host-side call)
-    const cudaError_t attr = cudaFuncSetAttribute(k_stats<NL>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (attr != cudaSuccess) return attr;
-    k_stats<NL><<<grid, kStatsWarps * 32, bytes, s>>>(a, st, lv);
+    k<<<grid, kStatsWarps * 32, bytes, s>>>(a, st, lv);
     return cudaGetLastError();
 }
 
@@ -929,6 +941,7 @@ static cg_status encode_levels(const cg_config *cfg, uint32_t levels, const floa
         a.esc_count = reinterpret_cast<uint32_t *>(w + L.esc_count[l]);
         a.words_count = reinterpret_cast<uint32_t *>(w + L.words_count[l]);
         a.scratch = reinterpret_cast<uint16_t *>(w + L.scratch);
+        a.sym = w + L.sym + l * L.sym_stride;
         a.region_words = L.region_words;
         a.dsizes = reinterpret_cast<cg_sizes *>(w + L.dsizes[l]);
         a.status = dev_status;
@@ -936,6 +949,8 @@ static cg_status encode_levels(const cg_config *cfg, uint32_t levels, const floa
     };
     StatsLevels lv;
     lv.raw_delta = lv.raw_anchor = nullptr;
+    lv.sym = w + L.sym;
+    lv.sym_stride = L.sym_stride;
     for (uint32_t l = 0; l < kMaxLevels; l++) {
         const EncArgs a = args(l < levels ? l : 0);
         lv.ftab[l] = a.ftab;
@@ -1150,6 +1165,8 @@ extern "C" cg_status cg_ablation(const cg_config *cfg, const uint16_t *kv, void 
     }
     lv.raw_delta = reinterpret_cast<uint32_t *>(w + W.raw_delta);
     lv.raw_anchor = reinterpret_cast<uint32_t *>(w + W.raw_anchor);
+    lv.sym = we + L.sym;  // written, not used
+    lv.sym_stride = L.sym_stride;
     auto *glob = reinterpret_cast<unsigned long long *>(w + W.global);
     CG_CUDA_TRY(cudaMemsetAsync(a.esc_count, 0, g.n_streams * 4u, s));
     CG_CUDA_TRY(cudaMemsetAsync(lv.raw_anchor, 0, g.n_tables * 256u * 4u, s));
