@@ -136,8 +136,13 @@ cg_status cg_status_from_flags(uint32_t flags);
 cg_status cg_encode_bounds(const cg_config *cfg, cg_bounds *b);
 
 /*
- * Encode kv (device, fp16 bits, [L][2][T][C] contiguous, 16-byte aligned:
- * it is read in 16-byte pieces) into `out`.
+ * Encode kv (fp16 bits, [L][2][T][C] contiguous, 16-byte aligned: it is read
+ * in 16-byte pieces) into `out`.  kv is memory of the current device, managed
+ * memory, or page-locked host memory mapped into the device's address space
+ * (cudaHostAlloc / cudaHostRegister): the kernels then read the cache straight
+ * from host memory, at the mapping's device address (cg_cache_source).  Any
+ * other pointer (unregistered host memory, another device's memory) is
+ * refused with CG_ERR_INVALID_ARG before any work is enqueued.
  * Implements the whole encoder: anchor scale and int8 anchors, delta
  * quantization with the layer's step (escape symbol 255 for |q| > 127),
  * per-(layer, K/V, channel) histograms normalized to 16-bit frequency tables,
@@ -145,7 +150,10 @@ cg_status cg_encode_bounds(const cg_config *cfg, cg_bounds *b);
  * the streams into one payload (the compression pipeline of
  * "CacheGen vs 传统量化KV缓存压缩技术深度对比与性能测试", §2.1).
  *   ws, ws_bytes: device workspace, at least cg_bounds.workspace_bytes,
- *                 256-byte aligned; contents on entry do not matter.
+ *                 256-byte aligned; contents on entry do not matter.  The
+ *                 workspace and every output section must be memory the
+ *                 device can use at that address (CG_ERR_INVALID_ARG
+ *                 otherwise, checked on the host before any work).
  *   out:          host struct of device pointers; anchors, scales, table_off,
  *                 stream_off and esc_off must hold their full sections,
  *                 tables/payload/escapes at least *_cap bytes/entries.
@@ -156,6 +164,16 @@ cg_status cg_encode_bounds(const cg_config *cfg, cg_bounds *b);
  */
 cg_status cg_encode(const cg_config *cfg, const uint16_t *kv, void *ws, size_t ws_bytes, const cg_encoded *out,
                     cg_sizes *sizes, uint32_t *dev_status, void *stream);
+
+/*
+ * Where the encoder's kernels would read a cache at kv (host query, no work
+ * enqueued): *mem_type receives the CUDA memory type of kv (0 unregistered
+ * host memory, 1 page-locked host memory, 2 device memory, 3 managed) and
+ * *device_view the address the kernels read, or NULL.  CG_OK when the
+ * current device can read it; CG_ERR_INVALID_ARG for null arguments or memory
+ * it cannot read; CG_ERR_CUDA when the query itself fails (no device).
+ */
+cg_status cg_cache_source(const void *kv, int *mem_type, const void **device_view);
 
 /*
  * Encode one cache at several quality levels in one call (at most 4): level

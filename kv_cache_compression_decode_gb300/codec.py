@@ -97,7 +97,8 @@ EXPORTS = ("cg_status_string", "cg_status_from_flags", "cg_encode_bounds", "cg_e
            "cg_decode_chunks_ws_bytes", "cg_decode_chunks", "cg_decode_chunks_noalloc", "cg_chunk_ranges",
            "cg_serialize",
            "cg_deserialize_header", "cg_deserialize", "cg_plan_levels", "cg_decode_paged",
-           "cg_encode_levels_ws_bytes", "cg_encode_levels", "cg_ablation_ws_bytes", "cg_ablation")
+           "cg_encode_levels_ws_bytes", "cg_encode_levels", "cg_ablation_ws_bytes", "cg_ablation",
+           "cg_cache_source")
 
 _lib = None
 
@@ -129,6 +130,7 @@ def lib() -> ct.CDLL:
         L.cg_ablation.argtypes = [ct.POINTER(cg_config), P, P, ct.c_size_t, P, P, P]
         L.cg_encode_levels.argtypes = [ct.POINTER(cg_config), U32, P, P, P, ct.c_size_t, P, P, P, P]
         L.cg_decode_paged.argtypes = [ct.POINTER(cg_config), ct.POINTER(cg_encoded), ct.POINTER(cg_paged_kv), P, P]
+        L.cg_cache_source.argtypes = [P, ct.POINTER(ct.c_int), ct.POINTER(ct.c_void_p)]
         for name in EXPORTS:
             if name not in ("cg_status_string",):
                 getattr(L, name).restype = ct.c_int
@@ -269,12 +271,21 @@ def alloc_encoded(cfg: Config, device="cuda", escapes_cap: Optional[int] = None,
                    e(max(escapes_cap, 1), torch.int32), e(b["n_streams"] + 1, torch.int32))
 
 
+def cache_source(kv: torch.Tensor):
+    """(status, CUDA memory type, address the encoder's kernels read) for a
+    cache tensor: device memory, or pinned host memory read over the host link."""
+    mt, view = ct.c_int(0), ct.c_void_p(None)
+    code = lib().cg_cache_source(kv.data_ptr(), ct.byref(mt), ct.byref(view))
+    return code, mt.value, view.value
+
+
 def cg_encode(cfg: Config, kv: torch.Tensor, ws: torch.Tensor, out: Encoded, sizes_host: ct.Structure,
               status: torch.Tensor, stream=None) -> None:
-    """Enqueue cg_encode.  kv: device fp16 [L][2][T][C]; ws: device uint8
+    """Enqueue cg_encode.  kv: fp16 [L][2][T][C] on the device, or in pinned
+    host memory (the kernels then read it over the host link); ws: device uint8
     workspace; sizes_host: a cg_sizes in (ideally pinned) host memory;
     status: device int32[1] cleared by the caller."""
-    assert kv.is_cuda and kv.dtype == torch.float16 and kv.is_contiguous()
+    assert (kv.is_cuda or kv.is_pinned()) and kv.dtype == torch.float16 and kv.is_contiguous()
     assert tuple(kv.shape) == (cfg.L, 2, cfg.T, cfg.C)
     code = lib().cg_encode(ct.byref(cfg.c()), kv.data_ptr(), ws.data_ptr(), ws.numel(), ct.byref(out.c()),
                            ct.byref(sizes_host), status.data_ptr(), _stream_ptr(stream))
@@ -456,16 +467,23 @@ class Encoder:
         return self.out.trimmed()
 
 
+def _cuda_device_of(kv: torch.Tensor) -> torch.device:
+    """The device that encodes kv: its own, or the current one for pinned host memory."""
+    return kv.device if kv.is_cuda else torch.device("cuda", torch.cuda.current_device())
+
+
 def encode(cfg: Config, kv: torch.Tensor, stream=None) -> Encoded:
-    """Encode a device cache and wait for it; raises on any device status."""
-    enc = Encoder(cfg, kv.device)
+    """Encode a cache (device or pinned host memory) and wait for it; raises
+    on any device status."""
+    dev = _cuda_device_of(kv)
+    enc = Encoder(cfg, dev)
     enc.launch(kv, stream)
-    torch.cuda.synchronize(kv.device)
+    torch.cuda.synchronize(dev)
     st = read_status(enc.status)
     if st == CG_ERR_RANGE and enc.sizes.n_escapes > enc.out.escapes.numel():
-        enc = Encoder(cfg, kv.device, escapes_cap=int(enc.sizes.n_escapes))
+        enc = Encoder(cfg, dev, escapes_cap=int(enc.sizes.n_escapes))
         enc.launch(kv, stream)
-        torch.cuda.synchronize(kv.device)
+        torch.cuda.synchronize(dev)
         st = read_status(enc.status)
     _check(st, "cg_encode (device)")
     return enc.result()
@@ -479,12 +497,12 @@ def cg_encode_levels_ws_bytes(cfg: Config, n_levels: int) -> int:
 
 def encode_levels(cfg: Config, kv: torch.Tensor, mults: Sequence[float], share_anchors: bool = True,
                   stream=None) -> List[Tuple[Config, Encoded]]:
-    """Encode a device cache at len(mults) quality levels with one call (one
+    """Encode a cache (device or pinned host memory) at len(mults) quality levels with one call (one
     statistics pass over the cache); level l uses cfg.step * mults[l].
     Returns (level config, trimmed object) per level; each object equals
     encode() with that level's steps.  With share_anchors the levels' objects
     share one anchors and one scales buffer."""
-    dev = kv.device
+    dev = _cuda_device_of(kv)
     n = len(mults)
     m32 = np.ascontiguousarray(mults, dtype=np.float32)
     cfgs = [Config(cfg.L, cfg.T, cfg.C, cfg.group_size, cfg.chunk_tokens, cfg.tokens_per_stream,
@@ -523,7 +541,7 @@ def ablation(cfg: Config, kv: torch.Tensor, stream=None) -> dict:
     """Ideal coded bits of the cache's delta symbols with one table per
     (layer, K/V, channel), per (layer, K/V) or for the whole cache, and of the
     anchors raw or entropy-coded (cg_ablation); adds bits/value per variant."""
-    dev = kv.device
+    dev = _cuda_device_of(kv)
     n = ct.c_size_t()
     _check(lib().cg_ablation_ws_bytes(ct.byref(cfg.c()), ct.byref(n)), "cg_ablation_ws_bytes")
     ws = torch.empty(n.value, dtype=torch.uint8, device=dev)

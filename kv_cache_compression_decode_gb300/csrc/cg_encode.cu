@@ -891,6 +891,53 @@ static cudaError_t launch_stats(dim3 grid, cudaStream_t s, const EncArgs &a, con
     return cudaGetLastError();
 }
 
+// Where the kernels of the current device read the cache at kv: memory of
+// the current device or managed memory (at kv), or page-locked host memory
+// mapped into the device's address space (at its device address, the same
+// as kv on a unified-addressing system: the cache is then read straight
+// from host memory, over the host link).  Anything else is refused before
+// any kernel could touch it.
+static cg_status cache_source(const void *kv, int *mem_type, const void **view) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, kv) != cudaSuccess) {
+        cudaGetLastError();
+        return CG_ERR_CUDA;
+    }
+    *mem_type = (int)at.type;
+    int dev = -1;
+    CG_CUDA_TRY(cudaGetDevice(&dev));
+    if ((at.type == cudaMemoryTypeDevice && at.device == dev) || at.type == cudaMemoryTypeManaged) {
+        *view = kv;
+        return CG_OK;
+    }
+    if (at.type == cudaMemoryTypeHost && at.devicePointer) {
+        *view = at.devicePointer;
+        return CG_OK;
+    }
+    return CG_ERR_INVALID_ARG;  // unregistered host memory, another device's memory
+}
+
+// Whether the kernels of the current device can use p as it is (a
+// workspace or an output section): device or managed memory, or host memory
+// mapped at the same address.
+static cg_status usable_as_is(const void *p) {
+    int mt = 0;
+    const void *view = nullptr;
+    const cg_status st = cache_source(p, &mt, &view);
+    if (st != CG_OK) return st;
+    return view == p ? CG_OK : CG_ERR_INVALID_ARG;
+}
+
+static cg_status outputs_usable(const cg_encoded &o) {
+    const void *ptrs[] = {o.anchors, o.scales, o.tables, o.table_off, o.payload, o.stream_off, o.escapes, o.esc_off};
+    for (const void *p : ptrs)
+        if (p) {
+            const cg_status st = usable_as_is(p);
+            if (st != CG_OK) return st;
+        }
+    return CG_OK;
+}
+
 // The encode of `levels` quality levels of one cache: level l uses the
 // configured steps times mult[l].  One statistics pass reads the cache for
 // every level (anchors, scales and all levels' tables); then each level is
@@ -916,6 +963,15 @@ static cg_status encode_levels(const cg_config *cfg, uint32_t levels, const floa
     if (bs != CG_OK) return bs;
     const WsLayout L = ws_layout(g, levels);
     if (ws_bytes < L.total) return CG_ERR_RANGE;
+    int mt = 0;
+    const void *view = nullptr;
+    const cg_status kr = cache_source(kv, &mt, &view);
+    if (kr != CG_OK) return kr;
+    if (reinterpret_cast<uintptr_t>(view) % 16u) return CG_ERR_INVALID_ARG;
+    kv = static_cast<const uint16_t *>(view);
+    cg_status us = usable_as_is(ws);  // the workspace and every output section
+    for (uint32_t l = 0; l < levels && us == CG_OK; l++) us = outputs_usable(outs[l]);
+    if (us != CG_OK) return us;
     uint8_t *w = static_cast<uint8_t *>(ws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -1125,6 +1181,13 @@ static AblationWs ablation_ws(const Geom &g) {
 
 }  // namespace cg
 
+extern "C" cg_status cg_cache_source(const void *kv, int *mem_type, const void **device_view) {
+    if (!kv || !mem_type || !device_view) return CG_ERR_INVALID_ARG;
+    *mem_type = 0;
+    *device_view = nullptr;
+    return cache_source(kv, mem_type, device_view);
+}
+
 extern "C" cg_status cg_ablation_ws_bytes(const cg_config *cfg, size_t *ws_bytes) {
     Geom g;
     if (!make_geom(cfg, &g) || !ws_bytes) return CG_ERR_INVALID_ARG;
@@ -1140,6 +1203,15 @@ extern "C" cg_status cg_ablation(const cg_config *cfg, const uint16_t *kv, void 
         return CG_ERR_INVALID_ARG;
     const AblationWs W = ablation_ws(g);
     if (ws_bytes < W.total) return CG_ERR_RANGE;
+    int mt = 0;
+    const void *view = nullptr;
+    const cg_status kr = cache_source(kv, &mt, &view);
+    if (kr != CG_OK) return kr;
+    if (reinterpret_cast<uintptr_t>(view) % 16u) return CG_ERR_INVALID_ARG;
+    kv = static_cast<const uint16_t *>(view);
+    cg_status us = usable_as_is(ws);
+    if (us == CG_OK) us = usable_as_is(out);
+    if (us != CG_OK) return us;
     uint8_t *w = static_cast<uint8_t *>(ws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const WsLayout L = ws_layout(g, 1);

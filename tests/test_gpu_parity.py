@@ -185,6 +185,33 @@ def test_corruption_is_flagged_not_faulted():
 
 
 @needs_gpu
+def test_encode_reads_pinned_host_cache():
+    """A cache in pinned host memory is read by the kernels over the host
+    link, and the object is the oracle's.  Pageable host memory is refused on
+    the host (INVALID_ARG, nothing enqueued) unless the system maps it."""
+    import ctypes as ct
+    L, T, Cc = 2, 700, 96
+    pc, oc = P.configs(L, T, Cc, 10, 256, 100)
+    x = synth.ar1_kv(L, T, Cc, 0.9, 2, seed=51)
+    oenc = O.encode(oc, x.numpy().view(np.uint16), nthreads=P.nthreads())
+    xp = x.pin_memory()
+    code, mem_type, view = C.cache_source(xp)
+    assert code == C.CG_OK and mem_type == 1 and view, (code, mem_type, view)
+    assert C.cache_source(x.cuda())[:2] == (C.CG_OK, 2)
+    enc = C.encode(pc, xp)
+    P.assert_same_object(P.gpu_to_np(enc), P.oracle_to_np(oenc), "encode from pinned host memory")
+    e2 = C.Encoder(pc, "cuda")
+    code = C.lib().cg_encode(ct.byref(pc.c()), x.data_ptr(), e2.ws.data_ptr(), e2.ws.numel(), ct.byref(e2.out.c()),
+                             ct.byref(e2.sizes), e2.status.data_ptr(), None)
+    if code == C.CG_OK:  # host memory the device reads through the system's page tables
+        torch.cuda.synchronize()
+        assert C.read_status(e2.status) == C.CG_OK
+        P.assert_same_object(P.gpu_to_np(e2.result()), P.oracle_to_np(oenc), "encode from pageable memory")
+    else:
+        assert code == C.CG_ERR_INVALID_ARG
+
+
+@needs_gpu
 def test_nonfinite_input_and_small_capacity_flagged():
     L, T, Cc = 1, 100, 64
     pc, _ = P.configs(L, T, Cc, 10, 0, 64)
