@@ -748,9 +748,26 @@ __device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *et
         } else {
             const float xa = __fmul_rn((float)*ap, sa);
             const uint32_t t_lo = max(gs + 1u, p0), t_hi = min(gs + G, p1);
-            for (uint32_t t = t_hi; t-- > t_lo;) {
-                const int q = quantize(ld_half(xp + (uint64_t)(t - gs) * C), xa, inv_step);
-                enc_step<true>(a, etab, symbol_of(q), q, lane, lt, S);
+            if (kG > 1) {  // the group's values loaded together: one memory latency, not one per step
+                float v[kV];
+#pragma unroll
+                for (uint32_t i = 0; i < kV; i++) {
+                    const uint32_t t = gs + 1u + i;
+                    v[i] = t >= t_lo && t < t_hi ? ld_half(xp + (uint64_t)(i + 1u) * C) : 0.f;
+                }
+#pragma unroll
+                for (uint32_t i = kV; i-- > 0;) {
+                    const uint32_t t = gs + 1u + i;
+                    if (t >= t_lo && t < t_hi) {
+                        const int q = quantize(v[i], xa, inv_step);
+                        enc_step<true>(a, etab, symbol_of(q), q, lane, lt, S);
+                    }
+                }
+            } else {
+                for (uint32_t t = t_hi; t-- > t_lo;) {
+                    const int q = quantize(ld_half(xp + (uint64_t)(t - gs) * C), xa, inv_step);
+                    enc_step<true>(a, etab, symbol_of(q), q, lane, lt, S);
+                }
             }
         }
         if (!has_next) break;
