@@ -249,8 +249,7 @@ __device__ __forceinline__ void count_rows(const Geom &g, const StatsLevels &lv,
     const uint32_t cnt = kM_ ? kM_ : m;
     const uint32_t C = kC ? kC : g.C;
     bool esc = false;
-#pragma unroll(kM_ ? kM_ : 3)
-    for (uint32_t i = 0; i < cnt; i++) {
+    auto row = [&](uint32_t i) {
         const float v = h2f(rows[i * kLanes]);
         nan_acc = __fmaf_rn(v, 0.f, nan_acc);  // v * 0 is NaN exactly for a NaN or infinite v
         const float d = __fsub_rn(v, xa);
@@ -261,6 +260,13 @@ __device__ __forceinline__ void count_rows(const Geom &g, const StatsLevels &lv,
             sp[l * lv.sym_stride + (uint64_t)i * C] = (uint8_t)s;
             esc = esc || s == kEsc;
         }
+    };
+    if constexpr (kM_ > 0) {
+#pragma unroll
+        for (uint32_t i = 0; i < kM_; i++) row(i);
+    } else {
+#pragma unroll 3
+        for (uint32_t i = 0; i < m; i++) row(i);
     }
     if (__any_sync(kFull, esc)) {
         for (uint32_t i = 0; i < cnt; i++) {
