@@ -116,20 +116,14 @@ __device__ __forceinline__ uint32_t symbol_of(int q) {
     return (uint32_t)(q + 127) <= 254u ? (uint32_t)(q + 127) : kEsc;
 }
 
-__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    return v;
-}
+// Warp reductions in one instruction each (integer add / min / max).
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) { return __reduce_add_sync(kFull, v); }
 
 // (value, symbol) argmax, smallest symbol on a tie.
 __device__ __forceinline__ void warp_argmax(uint32_t &v, uint32_t &s) {
-    for (int o = 16; o; o >>= 1) {
-        uint32_t ov = __shfl_xor_sync(kFull, v, o), os = __shfl_xor_sync(kFull, s, o);
-        if (ov > v || (ov == v && os < s)) {
-            v = ov;
-            s = os;
-        }
-    }
+    const uint32_t m = __reduce_max_sync(kFull, v);
+    s = __reduce_min_sync(kFull, v == m ? s : 0xFFFFFFFFu);
+    v = m;
 }
 
 constexpr int kStatsWarps = 16;
@@ -473,10 +467,8 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
         }
         N = warp_sum(N);
         const float rN = __frcp_rn(__uint2float_rn(N));  // used only when N > 0
-        for (int o = 16; o; o >>= 1) {
-            lo = min(lo, __shfl_xor_sync(kFull, lo, o));
-            hi = max(hi, __shfl_xor_sync(kFull, hi, o));
-        }
+        lo = __reduce_min_sync(kFull, lo);
+        hi = __reduce_max_sync(kFull, hi);
         any = __any_sync(kFull, any);
         if (!any) {
             if (lane == 0) {
