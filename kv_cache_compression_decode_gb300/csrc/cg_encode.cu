@@ -276,8 +276,9 @@ __device__ __forceinline__ void count_rows(const Geom &g, const StatsLevels &lv,
 // NL levels in one pass: their histograms side by side in dynamic shared
 // memory (NL x 32 KB), then the warps' staging rings; anchors and scales are
 // the same for every level.  kC = 1024 fixes the row stride of the symbol
-// stores at compile time (0: runtime).
-template <uint32_t NL, uint32_t kC>
+// and anchor stores at compile time (0: runtime); kRaw adds the raw counts
+// of the grouping ablation.
+template <uint32_t NL, uint32_t kC, bool kRaw>
 __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(EncArgs a, StepTable st, StatsLevels lv) {
     const Geom &g = a.g;
     const uint32_t grp = blockIdx.x, slice = blockIdx.y;
@@ -399,8 +400,8 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
                 const float v0 = h2f(gr[0]);
                 nan_acc = __fmaf_rn(v0, 0.f, nan_acc);
                 const float qa = anchor_q(v0, inv_sa);
-                a.anchors[(abase + p / 10u + h) * g.C + c] = (int8_t)qa;
-                if (lv.raw_anchor)
+                a.anchors[(abase + p / 10u + h) * (kC ? kC : g.C) + c] = (int8_t)qa;
+                if (kRaw)
                     atomicAdd(&lv.raw_anchor[((uint64_t)slice * g.C + c) * 256u + (uint32_t)((int)qa + 127)], 1u);
                 xa = __fmul_rn(qa, sa);
                 count_rows<NL, 9, kC>(g, lv, gr + kLanes, 9, xa, inv_step, hl, spt + (h * 10u + 1u) * (kC ? kC : g.C),
@@ -414,7 +415,7 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
                     nan_acc = __fmaf_rn(v, 0.f, nan_acc);
                     const float qa = anchor_q(v, inv_sa);
                     a.anchors[(abase + gi) * g.C + c] = (int8_t)qa;
-                    if (lv.raw_anchor)
+                    if (kRaw)
                         atomicAdd(&lv.raw_anchor[((uint64_t)slice * g.C + c) * 256u + (uint32_t)((int)qa + 127)],
                                   1u);
                     xa = __fmul_rn(qa, sa);
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
     const bool nonfinite = nan_acc != nan_acc;
     if (__any_sync(kFull, nonfinite) && lane == 0) flag(a.status, CG_ERR_NONFINITE);
     __syncthreads();
-    if (lv.raw_delta)  // level 0's counts, [table][symbol]
+    if (kRaw)  // level 0's counts, [table][symbol]
         for (uint32_t i = threadIdx.x; i < 256u * kLanes; i += blockDim.x)
             lv.raw_delta[((uint64_t)slice * g.C + grp * kLanes + (i & 31u)) * 256u + (i >> 5)] = hist[i];
 
@@ -898,7 +899,11 @@ static bool outputs_ok(const cg_encoded *out) {
 template <uint32_t NL>
 static cudaError_t launch_stats(dim3 grid, cudaStream_t s, const EncArgs &a, const StepTable &st, const StatsLevels &lv) {
     constexpr int bytes = (int)stats_smem_bytes<NL>();
-    auto k = NL == 1 && a.g.C == 1024 ? k_stats<NL, (NL == 1 ? 1024u : 0u)> : k_stats<NL, 0>;
+    // the raw counts (grouping ablation) only come with one level
+    auto k = NL > 1                ? k_stats<NL, 0, false>
+             : lv.raw_delta        ? (a.g.C == 1024 ? k_stats<1, 1024, true> : k_stats<1, 0, true>)
+             : a.g.C == 1024       ? k_stats<1, 1024, false>
+                                   : k_stats<1, 0, false>;
     // per device, so set before every launch (a host-side call)
     const cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (attr != cudaSuccess) return attr;
