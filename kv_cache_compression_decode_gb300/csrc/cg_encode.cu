@@ -811,16 +811,36 @@ __global__ void __launch_bounds__(kMaxEncWarps * 32, 3) k_encode(EncArgs a, Step
             a.tables[off] = (uint8_t)lo;
             a.tables[off + 1] = (uint8_t)hi;
         }
-        uint32_t cum = 0;
-        for (uint32_t s = lo; s <= hi; s++) {
-            uint32_t fm1 = a.ftab[table * 256u + s];
-            etab[s * kLanes + lane] = cum | (fm1 << 16);
-            etab[kEtabWords + s * kLanes + lane] = 0xFFFFFFFFu / (fm1 + 1u);
-            if (fits) {
-                a.tables[off + 2u + 2u * (s - lo)] = (uint8_t)(fm1 & 255u);
-                a.tables[off + 3u + 2u * (s - lo)] = (uint8_t)(fm1 >> 8);
+        // the lane's f - 1 row, 8 symbols (16 bytes) per load, the next load
+        // issued before the current 8 are used; compact entries are u16 when
+        // the tables section is 2-byte aligned (every table offset is even)
+        const uint16_t *frow = a.ftab + table * 256u;
+        const bool even = (reinterpret_cast<uintptr_t>(a.tables) & 1u) == 0;
+        uint32_t cum = 0, s0 = lo & ~7u;
+        uint4 w = *reinterpret_cast<const uint4 *>(frow + s0);
+        for (; s0 <= hi; s0 += 8u) {
+            const uint4 wn = s0 + 8u <= hi ? *reinterpret_cast<const uint4 *>(frow + s0 + 8u) : w;
+#pragma unroll
+            for (uint32_t i = 0; i < 8; i++) {
+                const uint32_t s = s0 + i;
+                const uint32_t word = i < 2 ? w.x : i < 4 ? w.y : i < 6 ? w.z : w.w;
+                const uint32_t fm1 = (i & 1u) ? word >> 16 : word & 0xFFFFu;
+                if (s >= lo && s <= hi) {
+                    etab[s * kLanes + lane] = cum | (fm1 << 16);
+                    etab[kEtabWords + s * kLanes + lane] = 0xFFFFFFFFu / (fm1 + 1u);
+                    if (fits) {
+                        const uint64_t at = off + 2u + 2u * (s - lo);
+                        if (even) {
+                            *reinterpret_cast<uint16_t *>(a.tables + at) = (uint16_t)fm1;
+                        } else {
+                            a.tables[at] = (uint8_t)(fm1 & 255u);
+                            a.tables[at + 1u] = (uint8_t)(fm1 >> 8);
+                        }
+                    }
+                    cum += fm1 + 1u;
+                }
             }
-            cum += fm1 + 1u;
+            w = wn;
         }
         s_scale[lane] = a.scales[(uint64_t)slice * g.C + c];
     }
