@@ -4,17 +4,22 @@
 // quantization, arithmetic coding with per-(layer, channel) statistics;
 // "CacheGen vs 传统量化KV缓存压缩技术深度对比与性能测试", §1 and §2.1):
 //   k_stats   one block per (32-channel group, layer, K/V): anchor absmax ->
-//             scale, int8 anchors, delta quantization (multiplication by the
-//             once-rounded inverse of the scale / step), shared-memory
-//             histograms (lane = channel, bank = lane: conflict-free
-//             atomics), escape counts per stream, normalization of the 32
-//             histograms to 16-bit frequency tables (warp-cooperative).
+//             scale; then every warp walks its own run of row tiles, staged
+//             by cp.async in a shared-memory ring: int8 anchors, delta
+//             quantization (multiplication by the once-rounded inverse of
+//             the scale / step), shared-memory histograms (lane = channel,
+//             bank = lane: conflict-free atomics), the u8 symbol of every
+//             delta (kept in the workspace for the coder), escape counts per
+//             stream; normalization of the 32 histograms to 16-bit frequency
+//             tables (warp-cooperative).
 //   k_scan    exclusive scans of table sizes, escape counts and stream sizes
 //             (block sums, then each block scans its tile).
 //   k_encode  one warp per stream (lane = channel): interleaved range ANS
-//             over the span's delta tokens in reverse, words written
-//             backwards into a per-stream scratch region, escapes placed
-//             from the end of the stream's escape range.
+//             over the stored symbols of the span's delta tokens in reverse
+//             (a group with an escape is quantized again from its fp16
+//             values, for the escape values), words written backwards into
+//             a per-stream scratch region, escapes placed from the end of
+//             the stream's escape range.
 //   k_pack    one warp per stream: copies the stream words into the
 //             payload at its prefix-sum offset, zero-padded to 16 bytes.
 #include <cuda_fp16.h>
@@ -639,6 +644,12 @@ struct EncStream {
     bool esc_bad;
 };
 
+// Quantized delta of v against anchor value xa: rint((v - xa) * RN(1/step)),
+// the statistics pass's arithmetic.
+__device__ __forceinline__ int quantize(float v, float xa, float inv_step) {
+    return __float2int_rn(__fmul_rn(__fsub_rn(v, xa), inv_step));
+}
+
 // One coder step of the lane's symbol, in reverse order: emit the low half
 // of the state if coding the symbol would overflow it (the warp's emitters
 // write in lane order), then x = floor(x / f) * 2^16 + x mod f + c.
@@ -646,10 +657,6 @@ struct EncStream {
 // s: the lane's symbol, q: its quantized delta (read only for an escape).
 // kHasEsc = false when no lane of the warp escapes in this step (the caller
 // checked).
-__device__ __forceinline__ int quantize(float v, float xa, float inv_step) {
-    return __float2int_rn(__fmul_rn(__fsub_rn(v, xa), inv_step));
-}
-
 template <bool kHasEsc>
 __device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab, uint32_t s, int q, uint32_t lane,
                                          uint32_t lt, EncStream &S) {
