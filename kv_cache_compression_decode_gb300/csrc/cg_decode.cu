@@ -248,13 +248,28 @@ struct Lut {
 
 // The warp's renormalization of the updated state xn into x: lanes whose
 // state fell below 2^16 take the next words of the stream in lane order.
+// Written in PTX so that the state takes its word under the predicate
+// (x = (x << 16) | w for the lanes that need one) instead of a select; the
+// ring load is unconditional and its index wraps within the ring.
+static_assert(kStateLow == 65536u && kRingWords == 1024u, "renorm constants");
 __device__ __forceinline__ void renorm(uint32_t &x, uint32_t xn, uint32_t &pw, const Lut &T, const uint16_t *ring) {
+    const uint32_t rs = (uint32_t)__cvta_generic_to_shared(ring);
     x = xn;
-    const bool need = x < kStateLow;
-    const uint32_t bal = __ballot_sync(kFull, need);
-    const uint32_t w = ring[(pw + __popc(bal & T.lt)) & (kRingWords - 1u)];
-    x = need ? __byte_perm(w, x, 0x5410) : x;  // (x << 16) | w
-    pw += __popc(bal);
+    asm("{\n\t.reg .pred p;\n\t.reg .b32 b, t, i, w;\n\t"
+        "setp.lt.u32 p, %0, 65536;\n\t"           // need = x < 2^16
+        "vote.sync.ballot.b32 b, p, 0xffffffff;\n\t"
+        "and.b32 t, b, %2;\n\t"                     // needing lanes below this one
+        "popc.b32 t, t;\n\t"
+        "add.u32 i, %1, t;\n\t"
+        "and.b32 i, i, 1023;\n\t"                   // ring index
+        "mad.lo.u32 i, i, 2, %3;\n\t"
+        "ld.shared.u16 w, [i];\n\t"
+        "@p prmt.b32 %0, w, %0, 0x5410;\n\t"        // (x << 16) | w
+        "popc.b32 t, b;\n\t"
+        "add.u32 %1, %1, t;\n\t}"                   // words taken by the warp
+        : "+r"(x), "+r"(pw)
+        : "r"(T.lt), "r"(rs)
+        : "memory");
 }
 
 // State update for the lane's symbol (r = slot - c_s, fm1 = f_s - 1, a
