@@ -624,19 +624,6 @@ constexpr int kMaxEncWarps = 12;
 constexpr uint32_t kEtabWords = 256 * kLanes;                   // one [symbol][lane] table
 constexpr uint32_t kEncSmemBytes = 2u * kEtabWords * 4u;         // coder table + reciprocals
 
-// floor(x / f) and x mod f for 1 <= f <= 65536 and x < f * 2^16, with
-// m = floor((2^32 - 1) / f) precomputed per symbol: x * m / 2^32 lies in
-// (x/f - 1, x/f], so its integer part is the quotient or one less, and one
-// correction makes it exact.
-__device__ __forceinline__ void udiv_magic(uint32_t x, uint32_t f, uint32_t m, uint32_t &q, uint32_t &r) {
-    q = __umulhi(x, m);
-    r = x - q * f;
-    if (r >= f) {
-        q += 1u;
-        r -= f;
-    }
-}
-
 struct EncStream {
     uint16_t *region;
     uint32_t top, xs, e_top;
@@ -673,21 +660,45 @@ __device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab,
             S.e_top -= ne;
         }
     }
-    const uint32_t e = etab[s * kLanes + lane], m = etab[kEtabWords + s * kLanes + lane];
-    const uint32_t f = (e >> 16) + 1u, cs = e & 0xFFFFu;
-    const bool emit = (S.xs >> 16) >= f;
-    const uint32_t mb = __ballot_sync(kFull, emit);
-    const uint32_t nem = __popc(mb);
-    // branch-free: every lane forms the address, the emitting lanes store
-    uint16_t *dst = S.region + (S.top - nem + __popc(mb & lt));
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.global.u16 [%0], %1;\n\t}"
-                 ::"l"(dst), "h"((unsigned short)(S.xs & 0xFFFFu)), "r"((uint32_t)emit)
+    // In PTX, so that emission, the state shift and the quotient correction
+    // run under predicates instead of selects.  Entry e = c | (f - 1) << 16
+    // and the reciprocal m = floor((2^32 - 1) / f) 32 KB further on.  The
+    // state emits its low half when x >= f * 2^16, i.e. x > (e | 0xFFFF)
+    // (never for f = 2^16); the emitting lanes write in lane order below the
+    // warp's top (branch-free: every lane forms the address).  Then, with
+    // x < f * 2^16, x * m / 2^32 lies in (x / f - 1, x / f], so q =
+    // umulhi(x, m) is floor(x / f) or one less; r = x - q f is corrected once,
+    // and x = q * 2^16 + r + c.
+    static_assert(kEtabWords * 4u == 32768u, "reciprocal table offset");
+    const uint32_t es = (uint32_t)__cvta_generic_to_shared(etab + s * kLanes + lane);
+    asm volatile("{\n\t.reg .pred p, k;\n\t.reg .b32 e, m, t, mb, f, q, r;\n\t.reg .b64 ad;\n\t"
+                 "ld.shared.u32 e, [%3];\n\t"
+                 "ld.shared.u32 m, [%3+32768];\n\t"
+                 "or.b32 t, e, 65535;\n\t"
+                 "setp.gt.u32 p, %0, t;\n\t"
+                 "vote.sync.ballot.b32 mb, p, 0xffffffff;\n\t"
+                 "popc.b32 t, mb;\n\t"
+                 "sub.u32 %1, %1, t;\n\t"
+                 "and.b32 t, mb, %4;\n\t"
+                 "popc.b32 t, t;\n\t"
+                 "add.u32 t, %1, t;\n\t"
+                 "mad.wide.u32 ad, t, 2, %2;\n\t"
+                 "@p st.global.u16 [ad], %0;\n\t"
+                 "@p shr.u32 %0, %0, 16;\n\t"
+                 "shr.u32 f, e, 16;\n\t"
+                 "add.u32 f, f, 1;\n\t"
+                 "mul.hi.u32 q, %0, m;\n\t"
+                 "mul.lo.u32 t, q, f;\n\t"
+                 "sub.u32 r, %0, t;\n\t"
+                 "setp.ge.u32 k, r, f;\n\t"
+                 "@k add.u32 q, q, 1;\n\t"
+                 "@k sub.u32 r, r, f;\n\t"
+                 "and.b32 t, e, 65535;\n\t"
+                 "add.u32 r, r, t;\n\t"
+                 "mad.lo.u32 %0, q, 65536, r;\n\t}"
+                 : "+r"(S.xs), "+r"(S.top)
+                 : "l"(S.region), "r"(es), "r"(lt)
                  : "memory");
-    S.xs = emit ? S.xs >> 16 : S.xs;
-    S.top -= nem;
-    uint32_t qd, rd;
-    udiv_magic(S.xs, f, m, qd, rd);
-    S.xs = (qd << 16) + rd + cs;
 }
 
 // Encode one stream: groups from the span's last to its first, each group's
