@@ -879,10 +879,20 @@ __global__ void __launch_bounds__(256) k_pack(EncArgs a) {
     const uint32_t cnt = a.words_count[k];
     const uint64_t off = a.stream_off[k], end = a.stream_off[k + 1];
     if (end > a.payload_cap) return;  // RANGE already flagged by the scan
+    // 16 bytes (8 words) per lane and pass: eight independent 2-byte loads
+    // (the words start at any 2-byte boundary of the scratch region), one
+    // 16-byte store (stream offsets and the payload are 16-byte aligned);
+    // words past the stream are the zero padding
     const uint16_t *src = a.scratch + k * a.region_words + (a.region_words - cnt);
-    uint16_t *dst = reinterpret_cast<uint16_t *>(a.payload + off);
-    const uint64_t n = (end - off) >> 1;
-    for (uint64_t i = lane; i < n; i += 32) dst[i] = i < cnt ? src[i] : (uint16_t)0;
+    uint4 *dst = reinterpret_cast<uint4 *>(a.payload + off);
+    const uint64_t n16 = (end - off) >> 4;
+    for (uint64_t j = lane; j < n16; j += 32) {
+        const uint64_t i0 = j * 8u;
+        uint32_t w[8];
+#pragma unroll
+        for (uint32_t i = 0; i < 8; i++) w[i] = i0 + i < cnt ? src[i0 + i] : 0u;
+        dst[j] = make_uint4(w[0] | w[1] << 16, w[2] | w[3] << 16, w[4] | w[5] << 16, w[6] | w[7] << 16);
+    }
 }
 
 __global__ void k_sizes(EncArgs a, uint64_t fixed_bytes) {
