@@ -190,6 +190,9 @@ __device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, floa
     const uint64_t b = o.table_off[table], e = o.table_off[table + 1];
     bool ok = e >= b + 2u && e <= o.tables_cap;
     uint32_t lo = 1, hi = 0;
+    if (ok)  // the lane's whole compact table into L1 first: one memory latency, not one per batch
+        for (uint64_t at = b & ~(uint64_t)127; at < e; at += 128)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(o.tables + at));
     if (ok) {
         const uint16_t h = *reinterpret_cast<const uint16_t *>(o.tables + b);
         lo = h & 255u;
@@ -200,12 +203,12 @@ __device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, floa
         ok = (e - b) == 2u + 2u * (hi - lo + 1u);
         const uint16_t *fm = reinterpret_cast<const uint16_t *>(o.tables + b + 2u);
         uint32_t cum = 0;
-        for (uint32_t s0 = lo; ok && s0 <= hi; s0 += 8) {
-            uint32_t v[8];
+        for (uint32_t s0 = lo; ok && s0 <= hi; s0 += 32) {
+            uint32_t v[32];
 #pragma unroll
-            for (int i = 0; i < 8; i++) v[i] = s0 + i <= hi ? fm[s0 + i - lo] : 0u;  // independent loads
+            for (int i = 0; i < 32; i++) v[i] = s0 + i <= hi ? fm[s0 + i - lo] : 0u;  // independent loads
 #pragma unroll
-            for (int i = 0; i < 8; i++) {
+            for (int i = 0; i < 32; i++) {
                 if (s0 + i > hi) break;
                 const uint32_t s = s0 + i, end = cum + v[i] + 1u;
                 if (end > kM) {
