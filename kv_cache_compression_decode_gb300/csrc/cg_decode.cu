@@ -1,8 +1,9 @@
 // cg_decode.cu -- GPU decoder of the KV-cache codec (sm_103a).
 //
 // One thread block per (object, layer, K/V, 32-channel group).  Warp 0 turns
-// the block's 32 compact frequency tables into shared-memory lookup tables,
-// laid out [entry][lane]:
+// the block's 32 compact frequency tables into shared-memory symbol tables,
+// then every warp fills a share of the bucket table; both are laid out
+// [entry][lane]:
 //   tab    [256][32] u32   c_s | (f_s - 1) << 16 (f - 1 keeps f = 65536, a
 //                          single-symbol table, within 16 bits)
 //   coarse [256][32] u16   bucket b (slots 256 b .. 256 b + 255): s0 << 8 | d,
@@ -88,7 +89,7 @@ static_assert((kRingSegs & (kRingSegs - 1u)) == 0, "slot = segment & (kRingSegs 
 constexpr uint32_t kTabOff = 0;                              // u32 [256][32]: c | (f - 1) << 16
 constexpr uint32_t kCoarseOff = kTabOff + 256 * kLanes * 4;  // u16 [256][32]: s0 << 8 | d (see top)
 constexpr uint32_t kDqOff = kCoarseOff + 256 * kLanes * 2;   // f32 [256]: float(s - 127) * step
-constexpr uint32_t kHiOff = kDqOff + 256 * 4;                // u32 [32]
+constexpr uint32_t kHiOff = kDqOff + 256 * 4;                // u32 [32]: lo << 16 | hi
 constexpr uint32_t kScaleOff = kHiOff + kLanes * 4;          // f32 [32]
 constexpr uint32_t kBadOff = kScaleOff + kLanes * 4;         // int
 constexpr uint32_t kBarOff = kBadOff + 16;                   // u64 [warps][kRingSegs]
@@ -175,8 +176,9 @@ __device__ __forceinline__ void ensure(Ring &R, Cursor &K, uint32_t need) {
 }
 
 
-// Warp 0: build the 32 lookup tables of (slice, grp) and the step's dequant
-// table in shared memory.
+// Warp 0: build the 32 symbol tables of (slice, grp), each lane's symbol
+// range (lo << 16 | hi) and the step's dequant table in shared memory; the
+// bucket table follows in fill_coarse.
 __device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, float step, uint8_t *smem,
                              uint32_t *status) {
     const Geom &g = o.g;
@@ -184,7 +186,6 @@ __device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, floa
     const uint32_t c = grp * kLanes + lane;
     const uint64_t table = (uint64_t)slice * g.C + c;
     uint32_t *tab = reinterpret_cast<uint32_t *>(smem + kTabOff);
-    uint16_t *coarse = reinterpret_cast<uint16_t *>(smem + kCoarseOff) + lane;
     float *dq = reinterpret_cast<float *>(smem + kDqOff);
     for (uint32_t s = lane; s < 256u; s += 32u) dq[s] = __fmul_rn(__int2float_rn((int)s - 127), step);
     const uint64_t b = o.table_off[table], e = o.table_off[table + 1];
@@ -198,7 +199,6 @@ __device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, floa
         lo = h & 255u;
         hi = h >> 8;
     }
-    uint32_t nb = 0;
     if (ok && lo <= hi) {
         ok = (e - b) == 2u + 2u * (hi - lo + 1u);
         const uint16_t *fm = reinterpret_cast<const uint16_t *>(o.tables + b + 2u);
@@ -216,10 +216,6 @@ __device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, floa
                     break;
                 }
                 tab[s * kLanes + lane] = cum | (v[i] << 16);
-                for (; nb < 256u && nb * 256u < end; nb++) {
-                    const uint32_t bend = (nb + 1u) * 256u;
-                    coarse[nb * kLanes] = (uint16_t)(s << 8 | (end < bend ? bend - end : 0u));
-                }
                 cum = end;
             }
         }
@@ -228,17 +224,51 @@ __device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, floa
     if (!ok || lo > hi) {
         // empty (no delta token in this call) or invalid: any slot resolves to
         // symbol 0 with f = 65536, and the block is skipped if invalid
-        for (; nb < 256u; nb++) coarse[nb * kLanes] = 0;
         tab[lane] = 0xFFFF0000u;
-        hi = 0;
+        lo = hi = 0;
     }
-    reinterpret_cast<uint32_t *>(smem + kHiOff)[lane] = hi;
+    reinterpret_cast<uint32_t *>(smem + kHiOff)[lane] = lo << 16 | hi;
     reinterpret_cast<float *>(smem + kScaleOff)[lane] = o.scales[table];
     const bool all_ok = __all_sync(kFull, ok);
     if (lane == 0) {
         *reinterpret_cast<int *>(smem + kBadOff) = !all_ok;
         if (!all_ok) flag_why(status, CG_ERR_CORRUPT, kWhyTable);
     }
+}
+
+// All warps: the bucket table.  Bucket b (slots 256 b .. 256 b + 255) of a
+// lane holds s0 << 8 | d, s0 the symbol containing slot 256 b -- the largest s
+// in [lo, hi] with c_s <= 256 b, found by a fixed 8-step binary search over
+// the lane's symbol table -- and d = 256 (b + 1) - (end of s0) when s0 ends
+// inside the bucket, else 0.  The buckets are spread over the block's warps.
+__device__ void fill_coarse(uint8_t *smem) {
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const uint32_t lh = reinterpret_cast<const uint32_t *>(smem + kHiOff)[lane];
+    const uint32_t hi = lh & 0xFFFFu, lo = lh >> 16;
+    const uint32_t *tab = reinterpret_cast<const uint32_t *>(smem + kTabOff) + lane;
+    uint16_t *coarse = reinterpret_cast<uint16_t *>(smem + kCoarseOff) + lane;
+    for (uint32_t b = warp; b < 256u; b += nw) {
+        const uint32_t slot = b * 256u;
+        uint32_t s = lo;  // c_lo = 0 <= slot
+#pragma unroll
+        for (uint32_t st = 128u; st; st >>= 1)
+            if (s + st <= hi && (tab[(s + st) * kLanes] & 0xFFFFu) <= slot) s += st;
+        const uint32_t e = tab[s * kLanes];
+        const uint32_t end = (e & 0xFFFFu) + (e >> 16) + 1u, bend = slot + 256u;
+        coarse[b * kLanes] = (uint16_t)(s << 8 | (end < bend ? bend - end : 0u));
+    }
+}
+
+// Every thread of the block: the lookup tables in shared memory.  Returns
+// false (for the whole block) when a table is malformed.
+__device__ __forceinline__ bool prepare_tables(const DecObj &o, uint32_t slice, uint32_t grp, float step,
+                                               uint8_t *smem, uint32_t *status) {
+    if ((threadIdx.x >> 5) == 0) build_tables(o, slice, grp, step, smem, status);
+    __syncthreads();
+    if (*reinterpret_cast<const int *>(smem + kBadOff)) return false;
+    fill_coarse(smem);
+    __syncthreads();
+    return true;
 }
 
 // Lane-private view of the block's tables.
@@ -420,7 +450,7 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
     T.tab = reinterpret_cast<const uint32_t *>(smem + kTabOff) + T.lane;
     T.coarse = reinterpret_cast<const uint16_t *>(smem + kCoarseOff) + T.lane;
     T.dq = reinterpret_cast<const float *>(smem + kDqOff);
-    T.hi = reinterpret_cast<const uint32_t *>(smem + kHiOff)[T.lane];
+    T.hi = reinterpret_cast<const uint32_t *>(smem + kHiOff)[T.lane] & 0xFFFFu;
     const uint32_t c = grp * kLanes + T.lane;
     const uint32_t ch = sp / g.spans_full, span = sp - ch * g.spans_full;
     const uint32_t c0 = ch * g.chunk, len = g.chunk_len(ch);
@@ -570,9 +600,7 @@ __global__ void __maxnreg__(kDecRegs) k_decode_all(DecObj o, StepTable st, uint1
     const uint32_t c = grp * kLanes + (threadIdx.x & 31u);
     const float step = st.v[slice >> 1];
     Ring R = make_ring(smem, nw);
-    if (warp == 0) build_tables(o, slice, grp, step, smem, status);
-    __syncthreads();
-    if (*reinterpret_cast<const int *>(smem + kBadOff)) return;
+    if (!prepare_tables(o, slice, grp, step, smem, status)) return;
     for (uint64_t sp = warp; sp < o.g.spans_total; sp += nw) {
         bool alive;
         if (kPaged) {
@@ -603,9 +631,7 @@ __global__ void __maxnreg__(kDecRegs) k_decode_jobs(const DecObj *objs, const De
     const uint32_t warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const float step = o.step[job.slice >> 1];
     Ring R = make_ring(smem, nw);
-    if (warp == 0) build_tables(o, job.slice, job.grp, step, smem, status);
-    __syncthreads();
-    if (*reinterpret_cast<const int *>(smem + kBadOff)) return;
+    if (!prepare_tables(o, job.slice, job.grp, step, smem, status)) return;
     for (uint32_t i = warp; i < job.span_count; i += nw) {
         const SpanRef sr = spans[job.span_begin + i];
         const RefDst rd = refs[sr.ref];
