@@ -357,18 +357,29 @@ __device__ __forceinline__ float rans_step(uint32_t &x, uint32_t &pw, const Lut 
     return dq;
 }
 
-// Common-path step: exact unless a lane of the warp holds a slot past a
-// second end inside its bucket or an escape.  Then it returns false with
-// nothing changed and the caller repeats the step with rans_step; keeping
-// that path out of the unrolled run leaves the run free of branches.
+// Common-path step: a lane whose slot lies past the end of the bucket's
+// carry symbol (a second end inside its bucket) takes the next symbol; if a
+// lane is still past its symbol's end (three or more ends), or one holds an
+// escape, the step returns false with nothing changed and the caller repeats
+// it with rans_step.  Keeping the walk out of the unrolled run leaves the run
+// free of loops.
 template <bool kHasEsc>
 __device__ __forceinline__ bool fast_step(uint32_t &x, uint32_t &pw, const Lut &T, const uint16_t *ring, float xa,
                                           uint16_t *dst) {
     const uint32_t e0 = T.coarse[((x >> 8) & 0xFFu) * kLanes];
-    const uint32_t s = (e0 + (x & 0xFFu)) >> 8;
-    const uint32_t e = T.tab[s * kLanes];
-    const uint32_t r = (x - e) & 0xFFFFu, fm1 = e >> 16;
-    if (__any_sync(kFull, kHasEsc ? (r > fm1 || s == kEsc) : r > fm1)) return false;
+    uint32_t s = (e0 + (x & 0xFFu)) >> 8;
+    uint32_t e = T.tab[s * kLanes];
+    uint32_t r = (x - e) & 0xFFFFu, fm1 = e >> 16;
+    if (__any_sync(kFull, r > fm1)) {  // a second end in the bucket: one more symbol
+        if (r > fm1) {
+            s++;
+            e = T.tab[s * kLanes];
+            r = (x - e) & 0xFFFFu;
+            fm1 = e >> 16;
+        }
+        if (__any_sync(kFull, r > fm1 || s > T.hi)) return false;
+    }
+    if (kHasEsc && __any_sync(kFull, s == kEsc)) return false;
     update(x, pw, T, ring, r, fm1);
     *dst = to_half(__fadd_rn(xa, T.dq[s]));
     return true;
