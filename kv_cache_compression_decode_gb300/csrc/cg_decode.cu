@@ -13,7 +13,7 @@
 // finds its symbol as (coarse + (slot & 255)) >> 8 -- the carry out of the low
 // byte steps past s0 exactly when the slot lies beyond s0's end -- takes one
 // more symbol in the rare bucket that holds a second end before the slot, and
-// walks on only with three or more (about 0.1% and 0.05% of slots); it then
+// walks on only with three or more (each a few lane-steps in a thousand); it then
 // updates its 32-bit range-ANS state, and the warp
 // renormalizes with one ballot (lanes take the next words in lane order).
 // Dequantization and the anchor add happen in fp32 and the fp16 result is
