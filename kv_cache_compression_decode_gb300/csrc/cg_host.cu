@@ -174,7 +174,7 @@ extern "C" cg_status cg_deserialize(const void *buf, size_t len, const cg_encode
     if (st != CG_OK) return st;
     if (!obj) return CG_ERR_INVALID_ARG;
     Geom g;
-    make_geom(&cfg, &g);
+    if (!make_geom(&cfg, &g)) return CG_ERR_CORRUPT;
     const SectionSizes z = section_sizes(g, sizes);
     if (obj->tables_cap < z.tables || obj->payload_cap < z.payload || obj->escapes_cap < sizes.n_escapes)
         return CG_ERR_RANGE;
