@@ -95,6 +95,18 @@ def test_null_buffers_rejected():
     assert C.lib().cg_decode_chunks_ws_bytes(None, 0, ct.byref(n)) == C.CG_ERR_INVALID_ARG
 
 
+def test_cache_source_host_checks():
+    """cg_cache_source refuses null arguments; without a usable device the
+    pointer query itself fails (CUDA error), and nothing is reported usable."""
+    mt, view = ct.c_int(7), ct.c_void_p(1)
+    assert C.lib().cg_cache_source(None, ct.byref(mt), ct.byref(view)) == C.CG_ERR_INVALID_ARG
+    assert C.lib().cg_cache_source(256, None, ct.byref(view)) == C.CG_ERR_INVALID_ARG
+    assert C.lib().cg_cache_source(256, ct.byref(mt), None) == C.CG_ERR_INVALID_ARG
+    if not torch.cuda.is_available():
+        code = C.lib().cg_cache_source(256, ct.byref(mt), ct.byref(view))
+        assert code == C.CG_ERR_CUDA and view.value is None
+
+
 def test_status_strings_and_flags():
     for code in range(7):
         assert C.cg_status_string(code)
