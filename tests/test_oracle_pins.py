@@ -274,6 +274,98 @@ def test_quantize_closed_form_delta_against_group_anchor():
     assert np.array_equal(y, x.view(np.uint16))  # exact grid: lossless
 
 
+# Hand-worked rounding cases (tests/golden/quantize_hand_examples.{json,txt}).
+# They fix what the closed-form grid cannot: ties are rounded to even, not
+# away from zero, and the quantizers multiply by the rounded inverse of the
+# scale / step instead of dividing by it.
+
+def _quant_examples():
+    return json.load(open(os.path.join(GOLD, "quantize_hand_examples.json")))["examples"]
+
+
+def _rn32(v: Fraction) -> Fraction:
+    """Nearest binary32 value to the rational v (normal range), ties to even."""
+    if v == 0:
+        return Fraction(0)
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fraction(2) ** (e - 23)
+    n = math.floor(a / ulp)
+    r = a / ulp - n
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return (n * ulp) if v > 0 else -(n * ulp)
+
+
+def _round_int(v: Fraction, half_even: bool) -> int:
+    n = math.floor(v)
+    r = v - n
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and (n % 2 == 1 if half_even else v > 0)):
+        n += 1
+    return n
+
+
+def _derive(ex, reading):
+    """(anchors, q) of an example by exact rational arithmetic under a reading:
+    'r' = the codec's (multiply by RN(1/s), ties to even), 'round_half_away',
+    'true_division'."""
+    vals = [Fraction(float.fromhex(v)) for v in ex["values"]]
+    G, step = ex["G"], Fraction(ex["step"])
+    half_even = reading != "round_half_away"
+    s = _rn32(max(abs(v) for i, v in enumerate(vals) if i % G == 0) / 127)
+    r_a, r = _rn32(1 / s), _rn32(1 / step)
+    anchors, q, xa = [], [], None
+    for i, v in enumerate(vals):
+        if i % G == 0:
+            t = _rn32(v / s) if reading == "true_division" else _rn32(v * r_a)
+            qa = max(-127, min(127, _round_int(t, half_even)))
+            anchors.append(qa)
+            xa = _rn32(qa * s)
+            q.append(None)
+        else:
+            d = _rn32(v - xa)
+            t = _rn32(d / step) if reading == "true_division" else _rn32(d * r)
+            q.append(_round_int(t, half_even))
+    return s, anchors, q
+
+
+@pytest.mark.parametrize("ex", _quant_examples(), ids=lambda e: e["name"][:40])
+def test_quantize_hand_examples_derivation(ex):
+    # the stored values follow the reading, and every other reading listed
+    # gives different codes, so each case catches that slip
+    s, anchors, q = _derive(ex, "r")
+    assert np.float32(float(s)).view(np.uint32) == int(ex["scale_bits"], 16)
+    assert anchors == ex["anchors"] and q == ex["q"]
+    for name, alt in ex["other_readings"].items():
+        _, a2, q2 = _derive(ex, name)
+        assert a2 == alt["anchors"] and q2 == alt.get("q", q2)
+        assert (a2, q2) != (anchors, q), name
+
+
+@pytest.mark.parametrize("ex", _quant_examples(), ids=lambda e: e["name"][:40])
+def test_quantize_hand_examples(ex):
+    vals = np.array([float.fromhex(v) for v in ex["values"]], dtype=np.float16)
+    assert vals.astype(np.float64).tolist() == ex["decimal"]  # exact fp16 inputs
+    T, G = len(vals), ex["G"]
+    cfg = O.Config(1, T, 32, G, T, T, np.array([ex["step"]], np.float32))
+    x = np.zeros((1, 2, T, 32), dtype=np.float16)
+    x[0, :, :, 0] = vals
+    scales = O.anchor_scales(cfg, x)
+    assert scales[0, :, 0].view(np.uint32).tolist() == [int(ex["scale_bits"], 16)] * 2
+    anchors, q = O.quantize(cfg, x, scales)
+    am = O.anchor_mask(cfg)
+    for kv in range(2):
+        assert anchors[0, kv, :, 0].tolist() == ex["anchors"]
+        assert q[0, kv, ~am, 0].tolist() == [v for v in ex["q"] if v is not None]
+    y = O.decode(cfg, O.encode(cfg, x))
+    expect = np.array(ex["recon"], dtype=np.float16).view(np.uint16)
+    assert np.array_equal(y[0, 0, :, 0], expect) and np.array_equal(y[0, 1, :, 0], expect)
+
+
 def _bound_check(cfg, x, y, scales):
     am = O.anchor_mask(cfg)
     xf = x.astype(np.float64)
