@@ -20,9 +20,14 @@
  *     compressed chunks (gptget.net page on the same paper, method details).
  *
  * Conventions for every entry point:
- *   - The library allocates nothing and keeps no global state.  Every buffer
- *     is owned by the caller.  "device" pointers are CUDA device memory of
- *     the current device, "host" pointers are CPU memory.
+ *   - The library allocates no device memory: every buffer is owned by the
+ *     caller.  "device" pointers are CUDA device memory of the current
+ *     device, "host" pointers are CPU memory.  Host-side state and scratch,
+ *     where a call has any, is said at the call: cg_decode_chunks plans its
+ *     descriptors in host heap memory that it frees before returning;
+ *     cg_decode_chunks_noalloc keeps a fixed device array, a static host
+ *     staging buffer and, per device, the array's device address for the
+ *     life of the process.  Every other call keeps no state between calls.
  *   - GPU work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and is asynchronous: outputs are valid after the stream is
  *     synchronized.
@@ -124,14 +129,18 @@ typedef struct {
     uint64_t payload_bytes, tables_bytes, n_escapes, total_bytes;
 } cg_sizes;
 
-/* Text for a status code.  Never NULL. */
+/* Text for a status code.  Never NULL.  (Status helper of this library; no
+ * passage of the CacheGen pages defines it.) */
 const char *cg_status_string(cg_status s);
 
-/* First error code set in a device status word (CG_OK when zero). */
+/* First error code set in a device status word (CG_OK when zero).  (Status
+ * helper of this library; no passage defines it.) */
 cg_status cg_status_from_flags(uint32_t flags);
 
 /* Fill *b with the sizes of every section and of the encode workspace for
- * `cfg`.  Host only; no CUDA call.  CG_ERR_INVALID_ARG on a bad config,
+ * `cfg`.  Sizing helper of this library (no passage of the pages defines it;
+ * the sections are those of the encoded object above).  Host only; no CUDA
+ * call.  CG_ERR_INVALID_ARG on a bad config,
  * CG_ERR_RANGE if an offset section would overflow its integer type. */
 cg_status cg_encode_bounds(const cg_config *cfg, cg_bounds *b);
 
@@ -172,6 +181,7 @@ cg_status cg_encode(const cg_config *cfg, const uint16_t *kv, void *ws, size_t w
  * *device_view the address the kernels read, or NULL.  CG_OK when the
  * current device can read it; CG_ERR_INVALID_ARG for null arguments or memory
  * it cannot read; CG_ERR_CUDA when the query itself fails (no device).
+ * (Query helper of this library; no passage of the pages defines it.)
  */
 cg_status cg_cache_source(const void *kv, int *mem_type, const void **device_view);
 
@@ -186,7 +196,8 @@ cg_status cg_cache_source(const void *kv, int *mem_type, const void **device_vie
  * sizes, each exactly what cg_encode gives with the level's steps.  outs[l]
  * may share the anchors and scales buffers of outs[0]; otherwise they get a
  * copy.  Every level's steps must be valid steps (> 2^-10, finite).
- *   ws: device, cg_encode_levels_ws_bytes() bytes, 256-byte aligned.
+ *   ws: device, cg_encode_levels_ws_bytes() bytes, 256-byte aligned
+ *       (cg_encode_levels_ws_bytes is its sizing helper, host only).
  */
 cg_status cg_encode_levels_ws_bytes(const cg_config *cfg, uint32_t n_levels, size_t *ws_bytes);
 cg_status cg_encode_levels(const cg_config *cfg, uint32_t n_levels, const float *mult, const uint16_t *kv, void *ws,
@@ -208,6 +219,25 @@ cg_status cg_encode_levels(const cg_config *cfg, uint32_t n_levels, const float 
 cg_status cg_decode(const cg_config *cfg, const cg_encoded *enc, uint16_t *kv_out, uint32_t *dev_status,
                     void *stream);
 
+/*
+ * Test hook for the device-side time-out path; no passage of the CacheGen
+ * pages defines it.  Every wait of the decoder on a bulk copy is bounded;
+ * this call makes such a wait run out on purpose, without a GPU fault or a
+ * hang, so that the path can be tested.  It decodes like cg_decode, except
+ * that the kernel never requests the bulk copy of ring segment 1 (stream
+ * bytes 256..511) of any stream, and each wait gives up after a few short
+ * polls instead of about a second.  A warp whose stream is longer than 256
+ * bytes therefore sees its wait run out: it ORs CG_ERR_TIMEOUT and
+ * diagnostic bit 22 into *dev_status, waits (bounded) for the copies it has
+ * issued, and takes no further stream; the kernel then returns.  Nothing is
+ * left in flight.  kv_out is undefined afterwards; the object, the
+ * destination and the context stay usable (a cg_decode of the same object
+ * that follows gives the normal output).  Arguments and host checks as for
+ * cg_decode.
+ */
+cg_status cg_test_decode_timeout(const cg_config *cfg, const cg_encoded *enc, uint16_t *kv_out,
+                                 uint32_t *dev_status, void *stream);
+
 /* One chunk to decode: chunk `chunk` of object `enc` (configured by `cfg`)
  * is written to dst, a device fp16 tensor [L][2][dst_tokens][C], at token
  * rows dst_token0 .. dst_token0 + chunk length - 1.  The encoded object's
@@ -222,7 +252,8 @@ typedef struct {
     uint32_t dst_token0;
 } cg_chunk_ref;
 
-/* Workspace bytes cg_decode_chunks needs for these refs.  Host only. */
+/* Workspace bytes cg_decode_chunks needs for these refs.  Sizing helper of
+ * this library (no passage defines it).  Host only. */
 cg_status cg_decode_chunks_ws_bytes(const cg_chunk_ref *refs, uint32_t n, size_t *ws_bytes);
 
 /*
@@ -251,8 +282,10 @@ cg_status cg_decode_chunks(const cg_chunk_ref *refs, uint32_t n, void *ws, size_
  * process exits.  It calls no cudaMalloc or cudaFree and no allocating
  * routine; the host side plans into static storage as well.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) and keeps it; make that first call before any
- *     stream capture.
+ *     (cudaGetSymbolAddress) and keeps it for the life of the process; make
+ *     that first call before any stream capture.  The kept address belongs
+ *     to the device's primary context: after cudaDeviceReset on that device
+ *     the library must be loaded again before this call is used.
  *   - Every call rewrites the array, so calls that overlap on the GPU race:
  *     issue them on one stream, or order them with events.  Calls from
  *     several host threads are serialized by a lock.
@@ -298,7 +331,10 @@ cg_status cg_decode_paged(const cg_config *cfg, const cg_encoded *enc, const cg_
 
 /* Where chunk `chunk` lives inside the per-chunk sections: byte ranges of
  * payload and anchors, entry range of escapes, and entry ranges of
- * stream_off / esc_off that describe it.  Host only; `off` arrays are host
+ * stream_off / esc_off that describe it.  Chunks are the unit that is stored
+ * and streamed ("CacheGen vs 传统量化KV缓存压缩技术深度对比与性能测试", §2.2:
+ * ~1.5K-token chunks sent one by one); the byte layout is this library's
+ * (per-chunk sections chunk-major, see the top of this file).  Host only; `off` arrays are host
  * copies of stream_off (u64) and esc_off (u32) of the object. */
 typedef struct {
     uint64_t stream_begin, stream_end;   /* stream indices */
@@ -310,7 +346,10 @@ cg_status cg_chunk_ranges(const cg_config *cfg, uint32_t chunk, const uint64_t *
                           cg_chunk_range *r);
 
 /*
- * Serialized object: a header (magic "CGKV", version, L, T, C, group_size,
+ * Serialized object, the stored form of an encoded context (the pages keep
+ * every chunk pre-encoded and stored until it is requested: "CacheGen vs
+ * 传统量化KV缓存压缩技术深度对比与性能测试", §2.2; the format itself is this
+ * library's).  A header (magic "CGKV", version, L, T, C, group_size,
  * chunk_tokens, tokens_per_stream, the L steps, section sizes) followed by
  * the sections of `obj` (host pointers) in the order listed at the top of
  * this file.  cg_serialize with buf == NULL reports the size in *len.
@@ -348,8 +387,8 @@ typedef struct {
 } cg_ablation_bits;
 
 /* kv as for cg_encode (16-byte aligned); ws: device, cg_ablation_ws_bytes()
- * bytes, 256-byte aligned; out: device, valid once the stream has completed;
- * dev_status as for cg_encode. */
+ * bytes (its sizing helper, host only), 256-byte aligned; out: device, valid
+ * once the stream has completed; dev_status as for cg_encode. */
 cg_status cg_ablation_ws_bytes(const cg_config *cfg, size_t *ws_bytes);
 cg_status cg_ablation(const cg_config *cfg, const uint16_t *kv, void *ws, size_t ws_bytes, cg_ablation_bits *out,
                       uint32_t *dev_status, void *stream);

@@ -98,7 +98,7 @@ EXPORTS = ("cg_status_string", "cg_status_from_flags", "cg_encode_bounds", "cg_e
            "cg_serialize",
            "cg_deserialize_header", "cg_deserialize", "cg_plan_levels", "cg_decode_paged",
            "cg_encode_levels_ws_bytes", "cg_encode_levels", "cg_ablation_ws_bytes", "cg_ablation",
-           "cg_cache_source")
+           "cg_cache_source", "cg_test_decode_timeout")
 
 _lib = None
 
@@ -116,6 +116,7 @@ def lib() -> ct.CDLL:
         L.cg_encode.argtypes = [ct.POINTER(cg_config), P, P, ct.c_size_t, ct.POINTER(cg_encoded),
                                 ct.POINTER(cg_sizes), P, P]
         L.cg_decode.argtypes = [ct.POINTER(cg_config), ct.POINTER(cg_encoded), P, P, P]
+        L.cg_test_decode_timeout.argtypes = [ct.POINTER(cg_config), ct.POINTER(cg_encoded), P, P, P]
         L.cg_decode_chunks_ws_bytes.argtypes = [ct.POINTER(cg_chunk_ref), U32, ct.POINTER(ct.c_size_t)]
         L.cg_decode_chunks.argtypes = [ct.POINTER(cg_chunk_ref), U32, P, ct.c_size_t, P, P]
         L.cg_decode_chunks_noalloc.argtypes = [ct.POINTER(cg_chunk_ref), U32, P, P]
@@ -299,6 +300,17 @@ def cg_decode(cfg: Config, enc: Encoded, kv_out: torch.Tensor, status: torch.Ten
     code = lib().cg_decode(ct.byref(cfg.c()), ct.byref(enc.c()), kv_out.data_ptr(), status.data_ptr(),
                            _stream_ptr(stream))
     _check(code, "cg_decode")
+
+
+def cg_test_decode_timeout(cfg: Config, enc: Encoded, kv_out: torch.Tensor, status: torch.Tensor,
+                           stream=None) -> None:
+    """Enqueue the decoder's time-out test kernel (a withheld ring segment and
+    short waits: every stream longer than 256 bytes reports CG_ERR_TIMEOUT)."""
+    assert kv_out.is_cuda and kv_out.dtype == torch.float16 and kv_out.is_contiguous()
+    assert tuple(kv_out.shape) == (cfg.L, 2, cfg.T, cfg.C)
+    code = lib().cg_test_decode_timeout(ct.byref(cfg.c()), ct.byref(enc.c()), kv_out.data_ptr(), status.data_ptr(),
+                                        _stream_ptr(stream))
+    _check(code, "cg_test_decode_timeout")
 
 
 def cg_decode_paged(cfg: Config, enc, pool: torch.Tensor, block_table: torch.Tensor, block_tokens: int,
@@ -535,6 +547,43 @@ def encode_levels(cfg: Config, kv: torch.Tensor, mults: Sequence[float], share_a
                    "n_escapes": int(sz.n_escapes), "total_bytes": int(sz.total_bytes)}
         res.append((c, o.trimmed()))
     return res
+
+
+class LevelEncoder:
+    """Holds the workspace, per-level outputs and pinned sizes of
+    cg_encode_levels for one config and set of step multipliers, so that the
+    call can be launched repeatedly without allocating (the levels share one
+    anchors and one scales buffer)."""
+
+    def __init__(self, cfg: Config, mults: Sequence[float], device="cuda", escapes_cap: Optional[int] = None):
+        self.cfg = cfg
+        self.n = len(mults)
+        self.mults = np.ascontiguousarray(mults, dtype=np.float32)
+        self.cfgs = [Config(cfg.L, cfg.T, cfg.C, cfg.group_size, cfg.chunk_tokens, cfg.tokens_per_stream,
+                            (np.asarray(cfg.step, np.float32) * m).astype(np.float32)) for m in self.mults]
+        self.ws = torch.empty(cg_encode_levels_ws_bytes(cfg, self.n), dtype=torch.uint8, device=device)
+        self.outs = [alloc_encoded(cfg, device, escapes_cap) for _ in range(self.n)]
+        for o in self.outs[1:]:
+            o.anchors, o.scales = self.outs[0].anchors, self.outs[0].scales
+        self.arr = (cg_encoded * self.n)(*[o.c() for o in self.outs])
+        self.sizes_buf = torch.zeros(4 * self.n, dtype=torch.int64, pin_memory=True)
+        self.sizes = (cg_sizes * self.n).from_address(self.sizes_buf.data_ptr())
+        self.status = new_status(device)
+
+    def launch(self, kv: torch.Tensor, stream=None) -> None:
+        code = lib().cg_encode_levels(ct.byref(self.cfg.c()), self.n, self.mults.ctypes.data, kv.data_ptr(),
+                                      self.ws.data_ptr(), self.ws.numel(), self.arr, ct.addressof(self.sizes),
+                                      self.status.data_ptr(), _stream_ptr(stream))
+        _check(code, "cg_encode_levels")
+
+    def results(self) -> List[Tuple[Config, Encoded]]:
+        """After the stream has completed: (level config, trimmed object) per level."""
+        res = []
+        for c, o, sz in zip(self.cfgs, self.outs, self.sizes):
+            o.sizes = {"payload_bytes": int(sz.payload_bytes), "tables_bytes": int(sz.tables_bytes),
+                       "n_escapes": int(sz.n_escapes), "total_bytes": int(sz.total_bytes)}
+            res.append((c, o.trimmed()))
+        return res
 
 
 def ablation(cfg: Config, kv: torch.Tensor, stream=None) -> dict:

@@ -77,6 +77,11 @@ constexpr uint32_t kRingWords = kSegWords * kRingSegs;  // 1024 words = 2 KB per
 constexpr uint32_t kAhead = 4;                          // segments requested ahead of the one awaited
 constexpr uint32_t kMaxRun = 9;                         // steps between ring checks (<= 288 words)
 constexpr uint32_t kSpinLimit = 1u << 14;               // x 64 us suspend hint: ~1 s bound per wait
+// Time-out test kernel (cg_test_decode_timeout): the bulk copy of this ring
+// segment of every stream is never issued, and a wait gives up after a few
+// polls.
+constexpr uint32_t kWithheldSeg = 1;
+constexpr uint32_t kTestSpinLimit = 16;
 // A run of kMaxRun steps reads words [pw, pw + R), R = 32 * kMaxRun.  The
 // run waits for segment k only when pw + R > k * W (W = kSegWords), and that
 // wait first requests segment k + kAhead into the slot of segment
@@ -142,9 +147,12 @@ struct Cursor {
     bool alive;
 };
 
+// kWithhold selects the time-out test kernel: segment kWithheldSeg is never
+// requested, so a wait for it runs out with nothing in flight.
+template <bool kWithhold>
 __device__ __forceinline__ void ring_issue(Ring &R, const Cursor &K, uint32_t k) {
     const uint32_t off = k * kSegBytes;
-    if (k >= K.nseg) return;
+    if (k >= K.nseg || (kWithhold && k == kWithheldSeg)) return;
     if ((threadIdx.x & 31u) == 0) {
         const uint32_t slot = k & (kRingSegs - 1u), bytes = min(kSegBytes, K.nbytes - off);
         fence_proxy_async();
@@ -154,23 +162,28 @@ __device__ __forceinline__ void ring_issue(Ring &R, const Cursor &K, uint32_t k)
 }
 
 // Waits (bounded) for segment k; false if the wait gave up.
+template <bool kWithhold>
 __device__ __forceinline__ bool ring_wait(Ring &R, uint32_t k) {
     const uint32_t slot = k & (kRingSegs - 1u);
     const uint32_t par = (R.phase >> slot) & 1u;
     bool ok = false;
-    for (uint32_t it = 0; it < kSpinLimit && !ok; it++) ok = mbar_try_wait(R.bar_s + 8u * slot, par);
+    for (uint32_t it = 0; it < (kWithhold ? kTestSpinLimit : kSpinLimit) && !ok; it++)
+        ok = mbar_try_wait(R.bar_s + 8u * slot, par);
     R.phase ^= 1u << slot;
     return __all_sync(kFull, ok);
 }
 
 // Make words [0, need) of the stream available.  Segment k + kAhead goes
 // into the slot of segment k + kAhead - kRingSegs, which the reads have
-// passed (the ring-window assertion above).
+// passed (the ring-window assertion above).  Once a wait has given up no
+// further segment is requested: the copies already issued are segments
+// [wseg, wseg + kAhead), which the end of the span waits for.
+template <bool kWithhold>
 __device__ __forceinline__ void ensure(Ring &R, Cursor &K, uint32_t need) {
-    while (K.avail < need && K.wseg < K.nseg) {
+    while (K.alive && K.avail < need && K.wseg < K.nseg) {
         __syncwarp();
-        ring_issue(R, K, K.wseg + kAhead);
-        K.alive = ring_wait(R, K.wseg) && K.alive;
+        ring_issue<kWithhold>(R, K, K.wseg + kAhead);
+        K.alive = ring_wait<kWithhold>(R, K.wseg);
         K.wseg++;
         K.avail = min(K.wseg * kSegWords, K.nw);
     }
@@ -448,7 +461,7 @@ struct PagedOut {
 
 // Decode stream (slice, grp, span sp) of object o into the rows of `O`.
 // kG = 10 / kC = 1024 select compile-time group size / row stride (0: runtime).
-template <bool kHasEsc, uint32_t kG, uint32_t kC, class Out>
+template <bool kHasEsc, uint32_t kG, uint32_t kC, class Out, bool kW>
 __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice, uint32_t grp, uint32_t sp,
                                                  float step, const uint8_t *smem, Ring &R, Out O, uint32_t *status,
                                                  uint64_t sb, uint64_t se, uint32_t eb, uint32_t ee,
@@ -480,8 +493,8 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
     K.alive = true;
     uint32_t x = 0, pw = 0, ep = eb;
     if (nsteps) {
-        for (uint32_t k = 0; k < kAhead; k++) ring_issue(R, K, k);
-        ensure(R, K, 2u * kLanes);
+        for (uint32_t k = 0; k < kAhead; k++) ring_issue<kW>(R, K, k);
+        ensure<kW>(R, K, 2u * kLanes);
         x = ((uint32_t)ring[2 * T.lane] << 16) | ring[2 * T.lane + 1];
         pw = 2u * kLanes;
     }
@@ -494,7 +507,7 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
     if (gp0) {  // head: the rest of a group whose anchor lies before the span
         const uint32_t cnt = min(G - gp0, p1 - p);
         for (uint32_t k = 0; k < cnt && K.alive && O.ok(); k++) {
-            if (k % kMaxRun == 0) ensure(R, K, pw + kLanes * min(kMaxRun, cnt - k));
+            if (k % kMaxRun == 0) ensure<kW>(R, K, pw + kLanes * min(kMaxRun, cnt - k));
             *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
         }
         p += cnt;
@@ -507,7 +520,7 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
         xa = __fmul_rn((float)qa_next, sa);
         if (p + G < p1) qa_next = arow[C];  // prefetch the next group's anchor
         *O.row(0, C) = to_half(xa);
-        if (kG) ensure(R, K, pw + kLanes * (kG - 1u));  // kG - 1 <= kMaxRun
+        if (kG) ensure<kW>(R, K, pw + kLanes * (kG - 1u));  // kG - 1 <= kMaxRun
         if (kG) {
             uint32_t k = 1;
 #pragma unroll
@@ -518,7 +531,7 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
                 *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
         } else {
             for (uint32_t k = 1; k < G; k++) {
-                if ((k - 1u) % kMaxRun == 0) ensure(R, K, pw + kLanes * min(kMaxRun, G - k));
+                if ((k - 1u) % kMaxRun == 0) ensure<kW>(R, K, pw + kLanes * min(kMaxRun, G - k));
                 *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
             }
         }
@@ -531,12 +544,13 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
         *O.row(0, C) = to_half(xa);
         const uint32_t cnt = p1 - p - 1u;
         for (uint32_t k = 1; k <= cnt && K.alive; k++) {
-            if ((k - 1u) % kMaxRun == 0) ensure(R, K, pw + kLanes * min(kMaxRun, cnt - k + 1u));
+            if ((k - 1u) % kMaxRun == 0) ensure<kW>(R, K, pw + kLanes * min(kMaxRun, cnt - k + 1u));
             *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
         }
     }
-    // drain copies still in flight before the ring is reused
-    for (uint32_t k = K.wseg; k < K.nseg && k < K.wseg + kAhead; k++) K.alive = ring_wait(R, k) && K.alive;
+    // drain the copies still in flight (also after a wait gave up) before the
+    // ring is reused or the block exits
+    for (uint32_t k = K.wseg; k < K.nseg && k < K.wseg + kAhead; k++) K.alive = ring_wait<kW>(R, k) && K.alive;
     if (!K.alive) {
         if (T.lane == 0) flag_why(status, CG_ERR_TIMEOUT, kWhyWait);
         return false;
@@ -558,9 +572,10 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
     return true;
 }
 
-// Returns false once a bounded wait of this warp has given up: the warp's
-// ring state is then unknown and it takes no further stream.
-template <class Out>
+// Returns false once a bounded wait of this warp has given up: the warp has
+// then waited (again bounded) for the copies it had issued, and it takes no
+// further stream.
+template <class Out, bool kW = false>
 __device__ bool decode_span(const DecObj &o, uint32_t slice, uint32_t grp, uint32_t sp, float step,
                             const uint8_t *smem, Ring &R, Out O, uint32_t *status) {
     const Geom &g = o.g;
@@ -580,7 +595,7 @@ __device__ bool decode_span(const DecObj &o, uint32_t slice, uint32_t grp, uint3
         return true;
     }
 #define CG_SPAN(E, GG, CC) \
-    decode_span_impl<E, GG, CC>(o, slice, grp, sp, step, smem, R, O, status, sb, se, eb, ee, nsteps)
+    decode_span_impl<E, GG, CC, Out, kW>(o, slice, grp, sp, step, smem, R, O, status, sb, se, eb, ee, nsteps)
     if (g.G == 10 && g.C == 1024) return ee != eb ? CG_SPAN(true, 10, 1024) : CG_SPAN(false, 10, 1024);
     if (g.G == 10) return ee != eb ? CG_SPAN(true, 10, 0) : CG_SPAN(false, 10, 0);
     return ee != eb ? CG_SPAN(true, 0, 0) : CG_SPAN(false, 0, 0);
@@ -603,8 +618,9 @@ __device__ __forceinline__ Ring make_ring(uint8_t *smem, uint32_t nwarps) {
     return R;
 }
 
-// kPaged: rows go to the blocks of `pd`, else to out[L][2][T][C].
-template <bool kPaged>
+// kPaged: rows go to the blocks of `pd`, else to out[L][2][T][C].  kW: the
+// time-out test kernel (a withheld ring segment, short waits).
+template <bool kPaged, bool kW = false>
 __global__ void __maxnreg__(kDecRegs) k_decode_all(DecObj o, StepTable st, uint16_t *out, PagedDst pd,
                                                    uint32_t *status) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -625,10 +641,10 @@ __global__ void __maxnreg__(kDecRegs) k_decode_all(DecObj o, StepTable st, uint1
             O.block_stride = pd.block_stride;
             O.ts = pd.token_stride;
             O.good = true;
-            alive = decode_span(o, slice, grp, (uint32_t)sp, step, smem, R, O, status);
+            alive = decode_span<PagedOut, kW>(o, slice, grp, (uint32_t)sp, step, smem, R, O, status);
         } else {
             const LinearOut<false> O{out + (uint64_t)slice * o.g.T * o.g.C, 0, c, nullptr};
-            alive = decode_span(o, slice, grp, (uint32_t)sp, step, smem, R, O, status);
+            alive = decode_span<LinearOut<false>, kW>(o, slice, grp, (uint32_t)sp, step, smem, R, O, status);
         }
         if (!alive) break;
     }
@@ -663,6 +679,9 @@ static cudaError_t set_smem_attrs() {
                                  (int)dec_smem_bytes(kMaxDecWarps));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_decode_jobs, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)dec_smem_bytes(kMaxDecWarps));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_decode_all<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)dec_smem_bytes(kMaxDecWarps));
     return e;
 }
@@ -773,6 +792,21 @@ extern "C" cg_status cg_decode(const cg_config *cfg, const cg_encoded *enc, uint
     CG_CUDA_TRY(set_smem_attrs());
     const uint32_t nwarps = warps_for(o.g.spans_total);
     k_decode_all<false><<<grid, nwarps * 32, dec_smem_bytes(nwarps), static_cast<cudaStream_t>(stream)>>>(
+        o, st, kv_out, PagedDst{}, dev_status);
+    CG_CUDA_TRY(cudaGetLastError());
+    return CG_OK;
+}
+
+extern "C" cg_status cg_test_decode_timeout(const cg_config *cfg, const cg_encoded *enc, uint16_t *kv_out,
+                                            uint32_t *dev_status, void *stream) {
+    DecObj o;
+    if (!fill_obj(cfg, enc, &o) || !kv_out) return CG_ERR_INVALID_ARG;
+    StepTable st;
+    for (uint32_t l = 0; l < o.g.L; l++) st.v[l] = cfg->step[l];
+    const dim3 grid(o.g.NG, o.g.n_slices);
+    CG_CUDA_TRY(set_smem_attrs());
+    const uint32_t nwarps = warps_for(o.g.spans_total);
+    k_decode_all<false, true><<<grid, nwarps * 32, dec_smem_bytes(nwarps), static_cast<cudaStream_t>(stream)>>>(
         o, st, kv_out, PagedDst{}, dev_status);
     CG_CUDA_TRY(cudaGetLastError());
     return CG_OK;

@@ -76,7 +76,7 @@ typedef struct {
 } cgo_config;
 
 typedef struct {
-    int8_t *anchors;      /* [L][2][A][C] */
+    int8_t *anchors;      /* [chunk][L][2][anchor rows of the chunk][C] */
     float *scales;        /* [L][2][C] */
     uint8_t *tables;      /* compact tables, see cgo_encode() */
     uint32_t *table_off;  /* [L*2*C + 1] byte offsets into tables */

@@ -189,7 +189,8 @@ def rans_decode(words: np.ndarray, steps: int, freq: np.ndarray, lo=None, hi=Non
 
 @dataclasses.dataclass
 class Encoded:
-    anchors: np.ndarray     # int8 [L][2][A][C]
+    anchors: np.ndarray     # int8, chunk-major [chunk][L][2][anchor rows of the chunk][C]
+                            # (the array is shaped [L][2][A][C] only for its size)
     scales: np.ndarray      # float32 [L][2][C]
     tables: np.ndarray      # uint8 [tables_bytes]
     table_off: np.ndarray   # uint32 [n_tables + 1]

@@ -91,6 +91,7 @@ def test_null_buffers_rejected():
     assert C.lib().cg_encode(ct.byref(cfg.c()), None, 256, 1 << 20, ct.byref(enc), ct.byref(sz), 0, None) \
         == C.CG_ERR_INVALID_ARG
     assert C.lib().cg_decode(ct.byref(cfg.c()), ct.byref(enc), 0, 0, None) == C.CG_ERR_INVALID_ARG
+    assert C.lib().cg_test_decode_timeout(ct.byref(cfg.c()), ct.byref(enc), 0, 0, None) == C.CG_ERR_INVALID_ARG
     n = ct.c_size_t()
     assert C.lib().cg_decode_chunks_ws_bytes(None, 0, ct.byref(n)) == C.CG_ERR_INVALID_ARG
 

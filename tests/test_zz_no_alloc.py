@@ -6,12 +6,14 @@ array inside libcg.
 
 This file is collected last on purpose, and it also passes when run alone in
 a fresh process.  It checks, through the C ABI, that two calls in a row give
-exactly the output of cg_decode_chunks (the workspace version), and that refs
-needing more descriptor space than the fixed array are refused."""
+exactly the output of cg_decode_chunks (the workspace version) and of the CPU
+oracle's decode, and that refs needing more descriptor space than the fixed
+array are refused."""
 import numpy as np
 import pytest
 import torch
 
+from oracle import oracle as O
 from kv_cache_compression_decode_gb300 import codec as C
 from kv_cache_compression_decode_gb300 import synth
 from tests import parity as P
@@ -21,11 +23,16 @@ needs_gpu = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CU
 
 
 def _levels(L, T, Cc, chunk, tps, seed):
-    x = synth.ar1_kv(L, T, Cc, 0.95, 1, seed=seed).cuda()
+    """Per quality level: (config, GPU object, oracle decode); every GPU object
+    is first checked byte for byte against the oracle's."""
+    x = synth.ar1_kv(L, T, Cc, 0.95, 1, seed=seed)
     objs = []
     for m in synth.LEVEL_MULTIPLIERS:
-        pc, _ = P.configs(L, T, Cc, 10, chunk, tps, m)
-        objs.append((pc, C.encode(pc, x)))
+        pc, oc = P.configs(L, T, Cc, 10, chunk, tps, m)
+        enc = C.encode(pc, x.cuda())
+        oenc = O.encode(oc, x.numpy().view(np.uint16))
+        P.assert_same_object(P.gpu_to_np(enc), P.oracle_to_np(oenc), f"level x{m}")
+        objs.append((pc, enc, O.decode(oc, oenc)))
     return objs
 
 
@@ -49,13 +56,17 @@ def test_noalloc_matches_workspace_decode_twice_in_a_row():
         ref_dst = torch.full((L, 2, T, Cc), float("nan"), dtype=torch.float16, device="cuda")
         refs = [C.ChunkRef(objs[lv][0], objs[lv][1], ch, ref_dst, ch * chunk) for ch, lv in enumerate(levels)]
         expect = _with_workspace(refs)
+        oracle = np.concatenate([objs[lv][2][:, :, ch * chunk:(ch + 1) * chunk] for ch, lv in enumerate(levels)],
+                                axis=2)
         out = torch.full((L, 2, T, Cc), float("nan"), dtype=torch.float16, device="cuda")
         refs_na = [C.ChunkRef(r.cfg, r.enc, r.chunk, out, r.dst_token0) for r in refs]
         st = C.new_status()
         C.cg_decode_chunks_noalloc(refs_na, st, stream)
         torch.cuda.synchronize()
         assert C.read_status(st) == C.CG_OK, f"call {call}"
-        assert np.array_equal(out.cpu().numpy().view(np.uint16), expect.cpu().numpy().view(np.uint16)), f"call {call}"
+        got = out.cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, expect.cpu().numpy().view(np.uint16)), f"call {call}"
+        assert np.array_equal(got, oracle), f"call {call} vs the oracle"
 
 
 @needs_gpu
