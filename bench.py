@@ -15,6 +15,13 @@ needed between steps.
 --impl reference times the CPU oracle (the plain C implementation the
 parity tests use) on a bounded sample of the same workload.
 
+--workload llama7b runs the same step on the Llama-7B-shaped cache (32
+layers x {K,V} x 4096 tokens x 32x128, 2 GiB; 4096 channels per token row).
+--workload mistral-mixed encodes the Mistral-7B-shaped cache (32 layers x
+{K,V} x 16384 tokens x 8x128, 1536-token chunks) at three quality levels
+(step x1, x2, x4) in one cg_encode_levels call, then decodes a seeded
+mixed-level chunk sequence in one cg_decode_chunks launch.
+
 --workload streamed measures the streamed batched decode instead: 64
 contexts of a Llama-34B-shaped cache (48 layers x {K,V} x 8x128, lengths
 uniform in 1.4K-16K tokens, about 112 GB of fp16), each encoded on the GPU
@@ -140,13 +147,13 @@ def barrier(dist, device):
 
 def cpu_baseline(workload, seconds_hint=20.0):
     """The oracle as it stands, on a bounded sample: encode + decode of the
-    first layers of the workload (enough (layer, K/V) slices for one thread
-    per host core, at most 8 layers)."""
+    first layers of the workload, enough (layer, K/V) slices that every host
+    core has one (the oracle threads over slices), on all host cores."""
     from oracle import oracle as O
     from kv_cache_compression_decode_gb300 import synth
 
     cores = os.cpu_count() or 1
-    L1 = max(1, min(8, workload.L, cores // 2))
+    L1 = max(1, min(workload.L, (cores + 1) // 2))
     x = synth.ar1_kv(L1, workload.T, workload.C, workload.rho, workload.n_outlier, workload.seed).numpy()
     oc = O.Config(L1, workload.T, workload.C, 10, workload.chunk, workload.tokens_per_stream,
                   O.layer_steps(workload.L)[:L1])
@@ -168,7 +175,7 @@ def cpu_baseline(workload, seconds_hint=20.0):
     t1 = time.perf_counter()
     O.decode(oc1, O.encode(oc1, x1, nthreads=1), nthreads=1)
     gbs1 = x1.nbytes / (time.perf_counter() - t1) / 1e9
-    return {"value": gbs, "unit": UNIT, "cores": min(cores, 2 * L1), "kind": "oracle",
+    return {"value": gbs, "unit": UNIT, "cores": min(cores, 2 * L1), "host_cores": cores, "kind": "oracle",
             "single_thread_value": gbs1,
             "sample": f"encode+decode of layers 0..{L1 - 1} ({2 * L1} slices of {workload.T} tokens x "
                       f"{workload.C} channels, {x16.nbytes / 1e6:.0f} MB fp16) of {workload.name}, {reps} reps, "
@@ -240,12 +247,120 @@ def run_streamed(args):
         "h2d_gbs": pick("h2d_gbs"), "h2d_bytes_per_step": runs[0]["h2d_bytes"], "h2d_ms": pick("h2d_ms"),
         "decode_ms": pick("decode_ms"), "overlap_efficiency": pick("overlap_efficiency"),
         "decode_gbs_fp16": round(fp16 / (pick("decode_ms") * 1e-3) / 1e9, 2),
+        "roofline": {"bound": "hbm", "kernel": "k_decode_jobs (sum of the stages' decode times)",
+                     "achieved": round((fp16 + runs[0]["h2d_bytes"]) / (pick("decode_ms") * 1e-3) / 1e9, 1),
+                     "peak": peaks()[0], "peak_kind": f"{peaks()[1]} hbm_gbs (burst copy)", "unit": "GB/s",
+                     "frac": round((fp16 + runs[0]["h2d_bytes"]) / (pick("decode_ms") * 1e-3) / 1e9 / peaks()[0], 4),
+                     "traffic": None, "algorithmic_bytes": fp16 + runs[0]["h2d_bytes"]},
         "last_context_equals_direct_decode": check, "gpu_launches": len(sd.stages) * args.steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
     if not check:
         raise SystemExit("streamed decode differs from the direct decode")
+
+
+def run_mixed(args):
+    """--workload mistral-mixed: three quality levels encoded in one call,
+    then one launch decoding a seeded mixed-level chunk sequence."""
+    from kv_cache_compression_decode_gb300 import codec as C
+    from kv_cache_compression_decode_gb300 import synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w = synth.MISTRAL7B
+    cfg = C.Config(w.L, w.T, w.C, w.group_size, w.chunk, w.tokens_per_stream, C.layer_steps(w.L))
+    kv = w.generate(device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n_chunks = (w.T + w.chunk - 1) // w.chunk
+    levels = synth.mixed_levels(n_chunks, seed=0)
+    le = C.LevelEncoder(cfg, synth.LEVEL_MULTIPLIERS, dev)
+    le.launch(kv, stream)
+    torch.cuda.synchronize(dev)
+    if C.read_status(le.status) == C.CG_ERR_RANGE:
+        le = C.LevelEncoder(cfg, synth.LEVEL_MULTIPLIERS, dev,
+                            escapes_cap=max(int(s.n_escapes) for s in le.sizes))
+        le.launch(kv, stream)
+        torch.cuda.synchronize(dev)
+    if C.read_status(le.status) != C.CG_OK:
+        raise C.CodecError(C.read_status(le.status), "cg_encode_levels")
+    objs = le.results()
+    out = torch.empty_like(kv)
+    refs = [C.ChunkRef(objs[q][0], objs[q][1], ch, out, ch * w.chunk) for ch, q in enumerate(levels)]
+    ws = torch.empty(C.cg_decode_chunks_ws_bytes(refs), dtype=torch.uint8, device=dev)
+    dstatus = C.new_status(dev)
+
+    # bytes the decode must read: each chunk's payload, escapes, anchors and
+    # stream offsets at its level, plus the tables and scales of every level used
+    comp = 0
+    for ch, q in enumerate(levels):
+        lc, o = objs[q]
+        r = C.cg_chunk_ranges(lc, ch, o.stream_off.cpu().numpy().view(np.uint64),
+                              o.esc_off.cpu().numpy().view(np.uint32))
+        comp += (r["payload_end"] - r["payload_begin"]) + 4 * (r["escape_end"] - r["escape_begin"]) \
+            + (r["anchor_end"] - r["anchor_begin"]) + 12 * (r["stream_end"] - r["stream_begin"])
+    for q in sorted(set(levels)):
+        o = objs[q][1]
+        comp += o.tables.numel() + 4 * o.table_off.numel() + 4 * o.scales.numel()
+    enc_out = sum(o.sizes["total_bytes"] for _, o in objs)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        le.launch(kv, stream)
+        if ev:
+            ev[1].record(stream)
+        C.cg_decode_chunks(refs, ws, dstatus, stream)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(dev.index) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    st = C.read_status(le.status) or C.read_status(dstatus)
+    if st != C.CG_OK:
+        raise C.CodecError(st, "timed steps")
+    total_ms = t0.elapsed_time(t1) / args.steps
+    enc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    fp16 = w.fp16_bytes
+    peak, peak_kind = peaks()
+    dec_ach = (fp16 + comp) / (dec_ms * 1e-3) / 1e9
+    enc_ach = (fp16 + enc_out) / (enc_ms * 1e-3) / 1e9
+    base = None if args.no_cpu_baseline else cpu_baseline(w)
+    line = {
+        "metric": METRIC, "value": round(fp16 / (total_ms * 1e-3) / 1e9, 2), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(total_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32+u32", "data": "synthetic",
+        "config": {"workload": f"{w.name}-3levels-mixed", "L": w.L, "T": w.T, "C": w.C,
+                   "group_size": w.group_size, "chunk_tokens": w.chunk, "tokens_per_stream": w.tokens_per_stream,
+                   "level_multipliers": list(synth.LEVEL_MULTIPLIERS), "chunk_levels": levels,
+                   "fp16_bytes": fp16, "step": "cg_encode_levels (x1, x2, x4 in one call) + cg_decode_chunks of "
+                                               "the mixed-level chunk sequence (one launch)",
+                   "l2": f"inputs ({fp16 / 1e9:.1f} GB) larger than L2; no flush"},
+        "decode": {"gbs_fp16": round(fp16 / (dec_ms * 1e-3) / 1e9, 2), "ms": round(dec_ms, 4),
+                   "hbm_frac": round(dec_ach / peak, 4), "compressed_bytes_read": comp},
+        "encode_levels": {"gbs_fp16": round(fp16 / (enc_ms * 1e-3) / 1e9, 2), "ms": round(enc_ms, 4),
+                          "hbm_frac": round(enc_ach / peak, 4), "compressed_bytes_written": enc_out},
+        "bits_per_value_per_level": [round(8 * o.sizes["total_bytes"] / w.values, 4) for _, o in objs],
+        "bits_per_value": round(8 * comp / w.values, 4),
+        "roofline": {"bound": "hbm", "kernel": "k_decode_jobs", "achieved": round(dec_ach, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "unit": "GB/s",
+                     "frac": round(dec_ach / peak, 4), "traffic": None, "algorithmic_bytes": fp16 + comp},
+        "cpu_baseline": base,
+        # one statistics pass, nine kernels per level (3 scans of 2, coder, pack, sizes), one decode
+        "gpu_launches": (KERNELS_PER_STEP + 9 * (len(objs) - 1)) * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
 
 
 def main():
@@ -256,7 +371,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--workload", default="llama70b", choices=["llama70b", "streamed"])
+    ap.add_argument("--workload", default="llama70b", choices=["llama70b", "llama7b", "mistral-mixed", "streamed"])
     ap.add_argument("--stream-tps", type=int, default=512, help="streamed: tokens per stream")
     ap.add_argument("--stream-cps", type=int, default=4, help="streamed: chunks per pipeline stage")
     ap.add_argument("--stream-slots", type=int, default=3, help="streamed: staging slots")
@@ -269,6 +384,9 @@ def main():
     if args.workload == "streamed":
         run_streamed(args)
         return
+    if args.workload == "mistral-mixed":
+        run_mixed(args)
+        return
 
     from kv_cache_compression_decode_gb300 import codec as C
     from kv_cache_compression_decode_gb300 import synth
@@ -276,12 +394,13 @@ def main():
     dist, rank, world, local = dist_init()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = synth.LLAMA70B
+    base_w = synth.LLAMA70B if args.workload == "llama70b" else synth.LLAMA7B
+    w = base_w
     if args.layers:
         import dataclasses
         w = dataclasses.replace(w, name=f"{w.name}-first{args.layers}layers", L=args.layers)
     cfg = C.Config(w.L, w.T, w.C, w.group_size, w.chunk, w.tokens_per_stream,
-                   C.layer_steps(synth.LLAMA70B.L)[: w.L])
+                   C.layer_steps(base_w.L)[: w.L])
     kv = w.generate(device=dev)
     enc = C.Encoder(cfg, dev)
     out = torch.empty_like(kv)
@@ -347,7 +466,7 @@ def main():
         host_kv.copy_(kv)
         nb = E2E_LAYER_BATCHES if w.L % E2E_LAYER_BATCHES == 0 else 1
         lb = w.L // nb
-        steps_all = C.layer_steps(synth.LLAMA70B.L)[: w.L]
+        steps_all = C.layer_steps(base_w.L)[: w.L]
         bcfg = [C.Config(lb, w.T, w.C, w.group_size, w.chunk, w.tokens_per_stream, steps_all[b * lb:(b + 1) * lb])
                 for b in range(nb)]
         bencs = [C.Encoder(c, dev) for c in bcfg]
@@ -409,7 +528,8 @@ def main():
             "config": {"workload": w.name, "L": w.L, "T": w.T, "C": w.C, "group_size": w.group_size,
                        "tokens_per_stream": w.tokens_per_stream, "steps_per_layer_third": [0.5, 1.0, 1.5],
                        "fp16_bytes": fp16, "step": "cg_encode + cg_decode of the whole cache",
-                       "l2": "inputs (5.4 GB) larger than L2; no flush", "parallelism": f"replicas x{world}"},
+                       "l2": f"inputs ({fp16 / 1e9:.1f} GB) larger than L2; no flush",
+                       "parallelism": f"replicas x{world}"},
             "decode": {"gbs_fp16": round(fp16 / (dec_ms * 1e-3) / 1e9, 2), "ms": round(dec_ms, 4),
                        "hbm_frac": round(dec_achieved / peak, 4)},
             "encode": {"gbs_fp16": round(fp16 / (enc_ms * 1e-3) / 1e9, 2), "ms": round(enc_ms, 4),
@@ -420,7 +540,8 @@ def main():
             "roofline": {"bound": "hbm", "kernel": "k_decode_all", "achieved": round(dec_achieved, 1),
                          "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (burst copy)", "unit": "GB/s",
                          "frac": round(dec_achieved / peak, 4),
-                         "traffic": (DECODE_TRAFFIC_BYTES if not args.layers and DECODE_TRAFFIC_BYTES else None),
+                         "traffic": (DECODE_TRAFFIC_BYTES if w is synth.LLAMA70B and DECODE_TRAFFIC_BYTES
+                                     else None),
                          "traffic_source": "ncu dram__bytes_read+write of an 8-layer launch x 10",
                          "algorithmic_bytes": dec_alg},
             "encode_roofline": {"bound": "hbm", "achieved": round(enc_achieved, 1), "peak": peak, "unit": "GB/s",
