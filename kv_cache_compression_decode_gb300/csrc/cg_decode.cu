@@ -291,7 +291,26 @@ struct Lut {
     const uint16_t *coarse;  // this lane's column: coarse[b * 32]
     const float *dq;
     uint32_t hi, lane, lt;
+    uint32_t tab_s, coarse_s, dq_s;  // the same three as shared-window addresses
 };
+
+// Loads from the shared window by 32-bit address.  The tables are written
+// before the block's barrier and only read afterwards.
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+    uint32_t v;
+    asm("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+    uint32_t v;
+    asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+    float v;
+    asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
 
 // The warp's renormalization of the updated state xn into x: lanes whose
 // state fell below 2^16 take the next words of the stream in lane order.
@@ -311,7 +330,7 @@ __device__ __forceinline__ void renorm(uint32_t &x, uint32_t xn, uint32_t &pw, c
         "and.b32 i, i, 1023;\n\t"                   // ring index
         "mad.lo.u32 i, i, 2, %3;\n\t"
         "ld.shared.u16 w, [i];\n\t"
-        "@p prmt.b32 %0, w, %0, 0x5410;\n\t"        // (x << 16) | w
+        "@p mad.lo.u32 %0, %0, 65536, w;\n\t"       // (x << 16) | w
         "popc.b32 t, b;\n\t"
         "add.u32 %1, %1, t;\n\t}"                   // words taken by the warp
         : "+r"(x), "+r"(pw)
@@ -376,26 +395,27 @@ __device__ __forceinline__ float rans_step(uint32_t &x, uint32_t &pw, const Lut 
 // lane is still past its symbol's end (three or more ends), or one holds an
 // escape, the step returns false with nothing changed and the caller repeats
 // it with rans_step.  Keeping the walk out of the unrolled run leaves the run
-// free of loops.
+// free of loops.  One vote per step covers both rare cases.
 template <bool kHasEsc>
 __device__ __forceinline__ bool fast_step(uint32_t &x, uint32_t &pw, const Lut &T, const uint16_t *ring, float xa,
                                           uint16_t *dst) {
-    const uint32_t e0 = T.coarse[((x >> 8) & 0xFFu) * kLanes];
+    const uint32_t e0 = lds_u16(T.coarse_s + __byte_perm(x, 0, 0x4441) * (kLanes * 2u));  // bucket: byte 1 of x
     uint32_t s = (e0 + (x & 0xFFu)) >> 8;
-    uint32_t e = T.tab[s * kLanes];
+    uint32_t e = lds_u32(T.tab_s + s * (kLanes * 4u));
+    float dq = lds_f32(T.dq_s + s * 4u);
     uint32_t r = (x - e) & 0xFFFFu, fm1 = e >> 16;
-    if (__any_sync(kFull, r > fm1)) {  // a second end in the bucket: one more symbol
-        if (r > fm1) {
+    if (__any_sync(kFull, kHasEsc ? (r > fm1 || s == kEsc) : r > fm1)) {
+        if (r > fm1) {  // a second end in the bucket: one more symbol
             s++;
-            e = T.tab[s * kLanes];
+            e = lds_u32(T.tab_s + s * (kLanes * 4u));
             r = (x - e) & 0xFFFFu;
             fm1 = e >> 16;
         }
-        if (__any_sync(kFull, r > fm1 || s > T.hi)) return false;
+        if (__any_sync(kFull, r > fm1 || s > T.hi || (kHasEsc && s == kEsc))) return false;
+        dq = lds_f32(T.dq_s + s * 4u);
     }
-    if (kHasEsc && __any_sync(kFull, s == kEsc)) return false;
     update(x, pw, T, ring, r, fm1);
-    *dst = to_half(__fadd_rn(xa, T.dq[s]));
+    *dst = to_half(__fadd_rn(xa, dq));
     return true;
 }
 
@@ -476,6 +496,9 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
     T.coarse = reinterpret_cast<const uint16_t *>(smem + kCoarseOff) + T.lane;
     T.dq = reinterpret_cast<const float *>(smem + kDqOff);
     T.hi = reinterpret_cast<const uint32_t *>(smem + kHiOff)[T.lane] & 0xFFFFu;
+    T.tab_s = smem_addr(T.tab);
+    T.coarse_s = smem_addr(T.coarse);
+    T.dq_s = smem_addr(T.dq);
     const uint32_t c = grp * kLanes + T.lane;
     const uint32_t ch = sp / g.spans_full, span = sp - ch * g.spans_full;
     const uint32_t c0 = ch * g.chunk, len = g.chunk_len(ch);
