@@ -661,7 +661,10 @@ __device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab,
         }
     }
     // In PTX, so that emission, the state shift and the quotient correction
-    // run under predicates instead of selects.  Entry e = c | (f - 1) << 16
+    // run under predicates instead of selects.  The emitted word is stored
+    // from a copy (the ballot's register, free by then): a store from the
+    // state register itself made the shift that follows wait until the store
+    // had read it.  Entry e = c | (f - 1) << 16
     // and the reciprocal m = floor((2^32 - 1) / f) 32 KB further on.  The
     // state emits its low half when x >= f * 2^16, i.e. x > (e | 0xFFFF)
     // (never for f = 2^16); the emitting lanes write in lane order below the
@@ -683,8 +686,9 @@ __device__ __forceinline__ void enc_step(const EncArgs &a, const uint32_t *etab,
                  "popc.b32 t, t;\n\t"
                  "add.u32 t, %1, t;\n\t"
                  "mad.wide.u32 ad, t, 2, %2;\n\t"
-                 "@p st.global.u16 [ad], %0;\n\t"
-                 "@p shr.u32 %0, %0, 16;\n\t"
+                 "and.b32 mb, %0, 65535;\n\t"               // the stored word in a register of its own,
+                 "@p st.global.u16 [ad], mb;\n\t"          // so the shift below need not wait for
+                 "@p shr.u32 %0, %0, 16;\n\t"              // the store to read the state
                  "shr.u32 f, e, 16;\n\t"
                  "add.u32 f, f, 1;\n\t"
                  "mul.hi.u32 q, %0, m;\n\t"
