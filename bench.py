@@ -199,7 +199,10 @@ def run_reference(args):
 
 
 def run_streamed(args):
-    """--workload streamed: decode pipelined against chunked H2D copies."""
+    """--workload streamed: decode pipelined against chunked H2D copies (one
+    GPU; under torchrun only rank 0 runs and reports)."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
     from kv_cache_compression_decode_gb300 import codec as C
     from kv_cache_compression_decode_gb300 import pipeline as PL
     from kv_cache_compression_decode_gb300 import synth
@@ -262,7 +265,10 @@ def run_streamed(args):
 
 def run_mixed(args):
     """--workload mistral-mixed: three quality levels encoded in one call,
-    then one launch decoding a seeded mixed-level chunk sequence."""
+    then one launch decoding a seeded mixed-level chunk sequence (one GPU;
+    under torchrun only rank 0 runs and reports)."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
     from kv_cache_compression_decode_gb300 import codec as C
     from kv_cache_compression_decode_gb300 import synth
 
