@@ -390,35 +390,6 @@ __device__ __forceinline__ float rans_step(uint32_t &x, uint32_t &pw, const Lut 
     return dq;
 }
 
-// Common-path step: a lane whose slot lies past the end of the bucket's
-// carry symbol (a second end inside its bucket) takes the next symbol; if a
-// lane is still past its symbol's end (three or more ends), or one holds an
-// escape, the step returns false with nothing changed and the caller repeats
-// it with rans_step.  Keeping the walk out of the unrolled run leaves the run
-// free of loops.  One vote per step covers both rare cases.
-template <bool kHasEsc>
-__device__ __forceinline__ bool fast_step(uint32_t &x, uint32_t &pw, const Lut &T, const uint16_t *ring, float xa,
-                                          uint16_t *dst) {
-    const uint32_t e0 = lds_u16(T.coarse_s + __byte_perm(x, 0, 0x4441) * (kLanes * 2u));  // bucket: byte 1 of x
-    uint32_t s = (e0 + (x & 0xFFu)) >> 8;
-    uint32_t e = lds_u32(T.tab_s + s * (kLanes * 4u));
-    float dq = lds_f32(T.dq_s + s * 4u);
-    uint32_t r = (x - e) & 0xFFFFu, fm1 = e >> 16;
-    if (__any_sync(kFull, kHasEsc ? (r > fm1 || s == kEsc) : r > fm1)) {
-        if (r > fm1) {  // a second end in the bucket: one more symbol
-            s++;
-            e = lds_u32(T.tab_s + s * (kLanes * 4u));
-            r = (x - e) & 0xFFFFu;
-            fm1 = e >> 16;
-        }
-        if (__any_sync(kFull, r > fm1 || s > T.hi || (kHasEsc && s == kEsc))) return false;
-        dq = lds_f32(T.dq_s + s * 4u);
-    }
-    update(x, pw, T, ring, r, fm1);
-    *dst = to_half(__fadd_rn(xa, dq));
-    return true;
-}
-
 // Output rows of one (layer, K/V) slice for the lane's channel.  Row k of a
 // group is token t + k; seek() places t, advance() moves it on.  C is the
 // row length of the [T][C] layout (a compile-time constant where known).
@@ -544,14 +515,48 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
         if (p + G < p1) qa_next = arow[C];  // prefetch the next group's anchor
         *O.row(0, C) = to_half(xa);
         if (kG) ensure<kW>(R, K, pw + kLanes * (kG - 1u));  // kG - 1 <= kMaxRun
-        if (kG) {
-            uint32_t k = 1;
-#pragma unroll
-            for (; k < (kG ? kG : 1u); k++)
-                if (!fast_step<kHasEsc>(x, pw, T, ring, xa, O.row(k, C))) break;
+        if constexpr (kG == 10) {
+            // The nine delta steps written out.  Per step: the bucket lookup,
+            // then one vote for the rare cases -- a slot past the end of the
+            // bucket's carry symbol (a second end inside its bucket) or an
+            // escape.  A lane past a second end takes the next symbol inline;
+            // if a lane is still past its symbol's end (three or more ends),
+            // or one holds an escape, the step jumps, with nothing changed,
+            // to the full steps, which finish the group.  Keeping the walk
+            // out of the written-out run leaves it free of loops, and the
+            // direct jump keeps the common path to the one vote's branch.
+            uint32_t k;
+#define CG_STEP(K)                                                                                          \
+    {                                                                                                       \
+        const uint32_t e0 = lds_u16(T.coarse_s + __byte_perm(x, 0, 0x4441) * (kLanes * 2u));                \
+        uint32_t s = (e0 + (x & 0xFFu)) >> 8;                                                               \
+        uint32_t e = lds_u32(T.tab_s + s * (kLanes * 4u));                                                  \
+        float dq = lds_f32(T.dq_s + s * 4u);                                                                \
+        uint32_t r = (x - e) & 0xFFFFu, fm1 = e >> 16;                                                      \
+        if (__any_sync(kFull, kHasEsc ? (r > fm1 || s == kEsc) : r > fm1)) {                                \
+            if (r > fm1) {                                                                                  \
+                s++;                                                                                        \
+                e = lds_u32(T.tab_s + s * (kLanes * 4u));                                                   \
+                r = (x - e) & 0xFFFFu;                                                                      \
+                fm1 = e >> 16;                                                                              \
+            }                                                                                               \
+            if (__any_sync(kFull, r > fm1 || s > T.hi || (kHasEsc && s == kEsc))) {                         \
+                k = K;                                                                                      \
+                goto cg_slow;                                                                               \
+            }                                                                                               \
+            dq = lds_f32(T.dq_s + s * 4u);                                                                  \
+        }                                                                                                   \
+        update(x, pw, T, ring, r, fm1);                                                                     \
+        *O.row(K, C) = to_half(__fadd_rn(xa, dq));                                                          \
+    }
+            CG_STEP(1) CG_STEP(2) CG_STEP(3) CG_STEP(4) CG_STEP(5) CG_STEP(6) CG_STEP(7) CG_STEP(8) CG_STEP(9)
+#undef CG_STEP
+            goto cg_done;
+        cg_slow:
 #pragma unroll 1
-            for (; k < (kG ? kG : 1u); k++)
+            for (; k < kG; k++)
                 *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
+        cg_done:;
         } else {
             for (uint32_t k = 1; k < G; k++) {
                 if ((k - 1u) % kMaxRun == 0) ensure<kW>(R, K, pw + kLanes * min(kMaxRun, G - k));
