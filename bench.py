@@ -52,9 +52,9 @@ KERNELS_PER_STEP = 11  # k_stats, 3 x (k_scan_sums + k_scan), k_encode, k_pack, 
 # end-to-end leg: the cache crosses the host link in this many layer batches
 E2E_LAYER_BATCHES = 8
 # DRAM bytes (read + write) of one k_decode_all launch on the full Llama-70B
-# workload: ncu capture of the first 8 layers (601.2 MB, grows with layers)
+# workload: ncu capture of the first 8 layers (600.4 MB, grows with layers)
 # scaled by 80/8.  Must be reset to None whenever k_decode_all changes.
-DECODE_TRAFFIC_BYTES = 601.2e6 * 10
+DECODE_TRAFFIC_BYTES = 600.4e6 * 10
 
 
 def peaks():
