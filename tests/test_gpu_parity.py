@@ -395,6 +395,29 @@ def test_multi_level_encode_matches_oracle_per_level(L, T, Cc, chunk, tps, share
                               O.decode(oc, oenc, nthreads=P.nthreads())), f"level x{m}"
 
 
+@needs_gpu
+def test_level_encoder_relaunches_give_the_oracle_objects():
+    """codec.LevelEncoder (the benchmark's repeated cg_encode_levels launch
+    into preallocated buffers) gives the oracle's object at every level, on
+    the first launch and again on a second launch into the same buffers."""
+    L, T, Cc, chunk, tps = 2, 900, 64, 300, 100
+    x = synth.ar1_kv(L, T, Cc, 0.95, 1, seed=63)
+    x[1, 0, 40, 3] = -21000.0  # escapes at every level
+    x16 = x.numpy().view(np.uint16)
+    pc, _ = P.configs(L, T, Cc, 10, chunk, tps)
+    le = C.LevelEncoder(pc, synth.LEVEL_MULTIPLIERS, "cuda")
+    xd = x.cuda()
+    for launch in range(2):
+        le.launch(xd)
+        torch.cuda.synchronize()
+        assert C.read_status(le.status) == C.CG_OK
+        for (lc, enc), m in zip(le.results(), synth.LEVEL_MULTIPLIERS):
+            _, oc = P.configs(L, T, Cc, 10, chunk, tps, m)
+            assert np.array_equal(lc.step, np.asarray(oc.step, np.float32))
+            oenc = O.encode(oc, x16)
+            P.assert_same_object(P.gpu_to_np(enc), P.oracle_to_np(oenc), f"launch {launch} level x{m}")
+
+
 def _bits(counts: np.ndarray) -> float:
     """Sum over rows of sum_s n_s log2(N / n_s), in float64."""
     c = counts.astype(np.float64)
