@@ -109,7 +109,10 @@ typedef struct {
 /* An encoded object.  For cg_encode these are device pointers to
  * caller-allocated outputs with the given capacities; for cg_decode they
  * point to a complete object in device memory; for cg_serialize /
- * cg_deserialize they point to host memory. */
+ * cg_deserialize they point to host memory.  The encode and decode calls
+ * take each section at an address aligned to its element type (2 bytes for
+ * tables, whose 16-bit entries sit at even offsets; 16 bytes for the payload)
+ * and refuse any other with CG_ERR_INVALID_ARG before anything is enqueued. */
 typedef struct {
     int8_t *anchors;
     float *scales;

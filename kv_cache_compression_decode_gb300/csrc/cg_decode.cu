@@ -190,97 +190,141 @@ __device__ __forceinline__ void ensure(Ring &R, Cursor &K, uint32_t need) {
 }
 
 
-// Warp 0: build the 32 symbol tables of (slice, grp), each lane's symbol
-// range (lo << 16 | hi) and the step's dequant table in shared memory; the
-// bucket table follows in fill_coarse.
-__device__ void build_tables(const DecObj &o, uint32_t slice, uint32_t grp, float step, uint8_t *smem,
-                             uint32_t *status) {
-    const Geom &g = o.g;
-    const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t c = grp * kLanes + lane;
-    const uint64_t table = (uint64_t)slice * g.C + c;
-    uint32_t *tab = reinterpret_cast<uint32_t *>(smem + kTabOff);
-    float *dq = reinterpret_cast<float *>(smem + kDqOff);
-    for (uint32_t s = lane; s < 256u; s += 32u) dq[s] = __fmul_rn(__int2float_rn((int)s - 127), step);
+// The block's tables, built in three phases separated by block barriers.
+// Lane = channel of the block's 32-channel group; the compact table of a
+// channel holds lo, hi (a byte each) and the 16-bit values f_s - 1 for
+// s = lo..hi, 2 + 2 (hi - lo + 1) bytes (2 bytes, lo > hi, when empty).
+//  1. Every warp reads the lane's offsets and header; warp w takes the
+//     batches j = w, w + nw, ... of 32 entries (entries 32 j .. 32 j + 31)
+//     and writes their frequency sum into a scratch row (the bucket table's
+//     space, which phase 3 fills).
+//  2. Each warp writes its batches' entries c_s | (f_s - 1) << 16, starting
+//     from the sum of the batches before them; warp 0 checks that the lane's
+//     frequencies add up to 65536 and writes lo / hi, the anchor scale and
+//     the block's verdict.
+//  3. Every warp fills a share of the bucket table.
+// The offsets alone bound every read (entries at even offsets inside the
+// section), so a malformed table is flagged, never read out of bounds.
+constexpr uint32_t kBatches = 256u / kLanes;
+
+__device__ __forceinline__ bool table_span(const DecObj &o, uint64_t table, uint64_t &at, uint32_t &n) {
     const uint64_t b = o.table_off[table], e = o.table_off[table + 1];
-    bool ok = e >= b + 2u && e <= o.tables_cap;
-    uint32_t lo = 1, hi = 0;
-    if (ok)  // the lane's whole compact table into L1 first: one memory latency, not one per batch
-        for (uint64_t at = b & ~(uint64_t)127; at < e; at += 128)
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(o.tables + at));
-    if (ok) {
-        const uint16_t h = *reinterpret_cast<const uint16_t *>(o.tables + b);
-        lo = h & 255u;
-        hi = h >> 8;
-    }
-    if (ok && lo <= hi) {
-        ok = (e - b) == 2u + 2u * (hi - lo + 1u);
-        const uint16_t *fm = reinterpret_cast<const uint16_t *>(o.tables + b + 2u);
-        uint32_t cum = 0;
-        for (uint32_t s0 = lo; ok && s0 <= hi; s0 += 32) {
-            uint32_t v[32];
-#pragma unroll
-            for (int i = 0; i < 32; i++) v[i] = s0 + i <= hi ? fm[s0 + i - lo] : 0u;  // independent loads
-#pragma unroll
-            for (int i = 0; i < 32; i++) {
-                if (s0 + i > hi) break;
-                const uint32_t s = s0 + i, end = cum + v[i] + 1u;
-                if (end > kM) {
-                    ok = false;
-                    break;
-                }
-                tab[s * kLanes + lane] = cum | (v[i] << 16);
-                cum = end;
-            }
-        }
-        ok = ok && cum == kM;
-    }
-    if (!ok || lo > hi) {
-        // empty (no delta token in this call) or invalid: any slot resolves to
-        // symbol 0 with f = 65536, and the block is skipped if invalid
-        tab[lane] = 0xFFFF0000u;
-        lo = hi = 0;
-    }
-    reinterpret_cast<uint32_t *>(smem + kHiOff)[lane] = lo << 16 | hi;
-    reinterpret_cast<float *>(smem + kScaleOff)[lane] = o.scales[table];
-    const bool all_ok = __all_sync(kFull, ok);
-    if (lane == 0) {
-        *reinterpret_cast<int *>(smem + kBadOff) = !all_ok;
-        if (!all_ok) flag_why(status, CG_ERR_CORRUPT, kWhyTable);
-    }
+    const bool ok = e >= b + 2u && e <= o.tables_cap && ((b | e) & 1u) == 0 && e - b <= 2u + 2u * 256u;
+    at = b;
+    n = ok ? (uint32_t)((e - b - 2u) >> 1) : 0u;
+    return ok;
 }
 
-// All warps: the bucket table.  Bucket b (slots 256 b .. 256 b + 255) of a
-// lane holds s0 << 8 | d, s0 the symbol containing slot 256 b -- the largest s
-// in [lo, hi] with c_s <= 256 b, found by a fixed 8-step binary search over
-// the lane's symbol table -- and d = 256 (b + 1) - (end of s0) when s0 ends
-// inside the bucket, else 0.  The buckets are spread over the block's warps.
-__device__ void fill_coarse(uint8_t *smem) {
-    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const uint32_t lh = reinterpret_cast<const uint32_t *>(smem + kHiOff)[lane];
-    const uint32_t hi = lh & 0xFFFFu, lo = lh >> 16;
-    const uint32_t *tab = reinterpret_cast<const uint32_t *>(smem + kTabOff) + lane;
-    uint16_t *coarse = reinterpret_cast<uint16_t *>(smem + kCoarseOff) + lane;
-    for (uint32_t b = warp; b < 256u; b += nw) {
-        const uint32_t slot = b * 256u;
-        uint32_t s = lo;  // c_lo = 0 <= slot
-#pragma unroll
-        for (uint32_t st = 128u; st; st >>= 1)
-            if (s + st <= hi && (tab[(s + st) * kLanes] & 0xFFFFu) <= slot) s += st;
-        const uint32_t e = tab[s * kLanes];
-        const uint32_t end = (e & 0xFFFFu) + (e >> 16) + 1u, bend = slot + 256u;
-        coarse[b * kLanes] = (uint16_t)(s << 8 | (end < bend ? bend - end : 0u));
-    }
-}
-
-// Every thread of the block: the lookup tables in shared memory.  Returns
-// false (for the whole block) when a table is malformed.
 __device__ __forceinline__ bool prepare_tables(const DecObj &o, uint32_t slice, uint32_t grp, float step,
                                                uint8_t *smem, uint32_t *status) {
-    if ((threadIdx.x >> 5) == 0) build_tables(o, slice, grp, step, smem, status);
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const uint64_t table = (uint64_t)slice * o.g.C + grp * kLanes + lane;
+    uint32_t *tab = reinterpret_cast<uint32_t *>(smem + kTabOff) + lane;
+    uint32_t *part = reinterpret_cast<uint32_t *>(smem + kCoarseOff) + lane;  // [kBatches][32] scratch
+    float *dq = reinterpret_cast<float *>(smem + kDqOff);
+    for (uint32_t s = threadIdx.x; s < 256u; s += blockDim.x) dq[s] = __fmul_rn(__int2float_rn((int)s - 127), step);
+
+    // phase 1
+    uint64_t at;
+    uint32_t n;
+    bool ok = table_span(o, table, at, n);
+    const uint16_t *fm = reinterpret_cast<const uint16_t *>(o.tables + at);  // header, then the entries
+    const uint32_t h = ok ? fm[0] : 0u;
+    const float sa = warp == 0 ? o.scales[table] : 0.f;
+    for (uint32_t j = warp; j < kBatches; j += nw) {
+        uint32_t sum = 0;
+#pragma unroll
+        for (uint32_t h0 = 0; h0 < kLanes; h0 += kLanes / 2) {
+            uint32_t v[kLanes / 2];
+#pragma unroll
+            for (uint32_t t = 0; t < kLanes / 2; t++) {
+                const uint32_t i = j * kLanes + h0 + t;
+                v[t] = i < n ? fm[1u + i] + 1u : 0u;
+            }
+#pragma unroll
+            for (uint32_t t = 0; t < kLanes / 2; t++) sum += v[t];
+        }
+        part[j * kLanes] = sum;
+    }
+    uint32_t lo = h & 255u, hi = h >> 8;
+    ok = ok && (lo <= hi ? n == hi - lo + 1u : n == 0u);
+    __syncthreads();
+
+    // phase 2
+    for (uint32_t j = warp; j < kBatches && ok && j * kLanes < n; j += nw) {
+        uint32_t cum = 0;
+        for (uint32_t i = 0; i < j; i++) cum += part[i * kLanes];
+#pragma unroll
+        for (uint32_t h0 = 0; h0 < kLanes; h0 += kLanes / 2) {
+            uint32_t v[kLanes / 2];
+#pragma unroll
+            for (uint32_t t = 0; t < kLanes / 2; t++) {
+                const uint32_t i = j * kLanes + h0 + t;
+                v[t] = i < n ? fm[1u + i] : 0u;
+            }
+#pragma unroll
+            for (uint32_t t = 0; t < kLanes / 2; t++) {
+                const uint32_t i = j * kLanes + h0 + t;
+                if (i < n) tab[(lo + i) * kLanes] = (cum & 0xFFFFu) | (v[t] << 16);
+                cum += v[t] + 1u;
+            }
+        }
+    }
+    if (warp == 0) {
+        uint32_t total = 0;
+#pragma unroll
+        for (uint32_t i = 0; i < kBatches; i++) total += part[i * kLanes];
+        ok = ok && (lo > hi || total == kM);
+        if (!ok || lo > hi) {
+            // empty (no delta token in this call) or invalid: any slot resolves to
+            // symbol 0 with f = 65536, and the block is skipped if invalid
+            tab[0] = 0xFFFF0000u;
+            lo = hi = 0;
+        }
+        reinterpret_cast<uint32_t *>(smem + kHiOff)[lane] = lo << 16 | hi;
+        reinterpret_cast<float *>(smem + kScaleOff)[lane] = sa;
+        const bool all_ok = __all_sync(kFull, ok);
+        if (lane == 0) {
+            *reinterpret_cast<int *>(smem + kBadOff) = !all_ok;
+            if (!all_ok) flag_why(status, CG_ERR_CORRUPT, kWhyTable);
+        }
+    }
     __syncthreads();
     if (*reinterpret_cast<const int *>(smem + kBadOff)) return false;
-    fill_coarse(smem);
+
+    // phase 3: bucket b (slots 256 b .. 256 b + 255) holds s0 << 8 | d, s0
+    // the symbol containing slot 256 b -- the largest s in [lo, hi] with
+    // c_s <= 256 b, found by a fixed 8-step binary search over the lane's
+    // symbol table -- and d = 256 (b + 1) - (end of s0) when s0 ends inside
+    // the bucket, else 0.  Four searches run side by side.
+    {
+        constexpr uint32_t kU = 4;
+        const uint32_t lh = reinterpret_cast<const uint32_t *>(smem + kHiOff)[lane];
+        const uint32_t lo3 = lh >> 16, hi3 = lh & 0xFFFFu;
+        uint16_t *coarse = reinterpret_cast<uint16_t *>(smem + kCoarseOff) + lane;
+        for (uint32_t b0 = warp; b0 < 256u; b0 += kU * nw) {
+            uint32_t sym[kU];
+#pragma unroll
+            for (uint32_t u = 0; u < kU; u++) sym[u] = lo3;  // c_lo = 0 <= any slot
+#pragma unroll
+            for (uint32_t st = 128u; st; st >>= 1) {
+#pragma unroll
+                for (uint32_t u = 0; u < kU; u++) {
+                    const uint32_t slot = (b0 + u * nw) * 256u;
+                    if (sym[u] + st <= hi3 && (tab[(sym[u] + st) * kLanes] & 0xFFFFu) <= slot) sym[u] += st;
+                }
+            }
+#pragma unroll
+            for (uint32_t u = 0; u < kU; u++) {
+                const uint32_t b = b0 + u * nw;
+                if (b < 256u) {
+                    const uint32_t e = tab[sym[u] * kLanes];
+                    const uint32_t end = (e & 0xFFFFu) + (e >> 16) + 1u, bend = b * 256u + 256u;
+                    coarse[b * kLanes] = (uint16_t)(sym[u] << 8 | (end < bend ? bend - end : 0u));
+                }
+            }
+        }
+    }
     __syncthreads();
     return true;
 }
@@ -719,7 +763,7 @@ static bool fill_obj(const cg_config *cfg, const cg_encoded *enc, DecObj *o) {
     if (!enc->anchors || !enc->scales || !enc->tables || !enc->table_off || !enc->stream_off || !enc->esc_off)
         return false;
     if ((!enc->payload && enc->payload_cap) || (!enc->escapes && enc->escapes_cap)) return false;
-    if (reinterpret_cast<uintptr_t>(enc->payload) % 16u) return false;
+    if (!sections_aligned(*enc)) return false;
     o->anchors = enc->anchors;
     o->scales = enc->scales;
     o->tables = enc->tables;

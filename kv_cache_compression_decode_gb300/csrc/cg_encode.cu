@@ -834,10 +834,9 @@ __global__ void __launch_bounds__(kMaxEncWarps * 32, 3) k_encode(EncArgs a, Step
             a.tables[off + 1] = (uint8_t)hi;
         }
         // the lane's f - 1 row, 8 symbols (16 bytes) per load, the next load
-        // issued before the current 8 are used; compact entries are u16 when
-        // the tables section is 2-byte aligned (every table offset is even)
+        // issued before the current 8 are used; compact entries are u16 (the
+        // tables section is 2-byte aligned and every table offset is even)
         const uint16_t *frow = a.ftab + table * 256u;
-        const bool even = (reinterpret_cast<uintptr_t>(a.tables) & 1u) == 0;
         uint32_t cum = 0, s0 = lo & ~7u;
         uint4 w = *reinterpret_cast<const uint4 *>(frow + s0);
         for (; s0 <= hi; s0 += 8u) {
@@ -850,15 +849,7 @@ __global__ void __launch_bounds__(kMaxEncWarps * 32, 3) k_encode(EncArgs a, Step
                 if (s >= lo && s <= hi) {
                     etab[s * kLanes + lane] = cum | (fm1 << 16);
                     etab[kEtabWords + s * kLanes + lane] = 0xFFFFFFFFu / (fm1 + 1u);
-                    if (fits) {
-                        const uint64_t at = off + 2u + 2u * (s - lo);
-                        if (even) {
-                            *reinterpret_cast<uint16_t *>(a.tables + at) = (uint16_t)fm1;
-                        } else {
-                            a.tables[at] = (uint8_t)(fm1 & 255u);
-                            a.tables[at + 1u] = (uint8_t)(fm1 >> 8);
-                        }
-                    }
+                    if (fits) *reinterpret_cast<uint16_t *>(a.tables + off + 2u + 2u * (s - lo)) = (uint16_t)fm1;
                     cum += fm1 + 1u;
                 }
             }
@@ -944,8 +935,7 @@ extern "C" cg_status cg_encode_bounds(const cg_config *cfg, cg_bounds *b) {
 
 static bool outputs_ok(const cg_encoded *out) {
     return out && out->anchors && out->scales && out->tables && out->table_off && out->stream_off && out->esc_off &&
-           (out->payload || !out->payload_cap) && (out->escapes || !out->escapes_cap) &&
-           reinterpret_cast<uintptr_t>(out->payload) % 16u == 0;
+           (out->payload || !out->payload_cap) && (out->escapes || !out->escapes_cap) && sections_aligned(*out);
 }
 
 template <uint32_t NL>

@@ -101,6 +101,15 @@ __device__ inline void flag_why(uint32_t *status, cg_status code, uint32_t why) 
     if (status) atomicOr(status, (1u << (uint32_t)code) | why);
 }
 
+// Each section of an object at an address aligned to its element type, the
+// payload to 16 bytes (the decoder's bulk copies): the kernels read and
+// write them by element.
+inline bool sections_aligned(const cg_encoded &o) {
+    const auto mis = [](const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1u)) != 0; };
+    return !(mis(o.scales, 4) || mis(o.tables, 2) || mis(o.table_off, 4) || mis(o.payload, 16) ||
+             mis(o.stream_off, 8) || mis(o.escapes, 4) || mis(o.esc_off, 4));
+}
+
 __device__ inline uint32_t lanemask_lt() {
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));

@@ -96,6 +96,43 @@ def test_null_buffers_rejected():
     assert C.lib().cg_decode_chunks_ws_bytes(None, 0, ct.byref(n)) == C.CG_ERR_INVALID_ARG
 
 
+_SECTIONS = ["anchors", "scales", "tables", "table_off", "payload", "stream_off", "escapes", "esc_off"]
+_ALIGN = {"scales": 4, "tables": 2, "table_off": 4, "payload": 16, "stream_off": 8, "escapes": 4, "esc_off": 4}
+
+
+def _fake_object(shift=None):
+    """A cg_encoded of made-up, never dereferenced addresses (each 4 KiB
+    apart), optionally with one section moved off its alignment."""
+    ptrs = {f: (1 << 24) + 4096 * i for i, f in enumerate(_SECTIONS)}
+    if shift:
+        ptrs[shift[0]] += shift[1]
+    return C.cg_encoded(*[ptrs[f] for f in _SECTIONS], 1 << 16, 1 << 20, 1 << 16)
+
+
+@pytest.mark.parametrize("field,off", [(f, o) for f, a in _ALIGN.items() for o in sorted({1, a // 2})])
+def test_misaligned_sections_refused_on_host(field, off):
+    """Each section sits at an address aligned to its element type (the
+    payload to 16 bytes).  A misaligned one is refused before anything is
+    enqueued.  Controls with every section aligned show that the refusal
+    comes from the alignment: the encoder then stops at its workspace-size
+    check (RANGE, still on the host), and the chunk planner, which runs on
+    the host alone, accepts the object."""
+    cfg = _cfg(L=2, T=100, C=64, chunk_tokens=50, tokens_per_stream=50)
+    sz = C.cg_sizes()
+    kv = ws = dst = 1 << 30
+    ok, bad = _fake_object(), _fake_object((field, off))
+    assert C.lib().cg_encode(ct.byref(cfg.c()), kv, ws, 1, ct.byref(ok), ct.byref(sz), 0, None) == C.CG_ERR_RANGE
+    assert C.lib().cg_encode(ct.byref(cfg.c()), kv, ws, 1, ct.byref(bad), ct.byref(sz), 0, None) \
+        == C.CG_ERR_INVALID_ARG
+    n = ct.c_size_t()
+    for enc, want in ((ok, C.CG_OK), (bad, C.CG_ERR_INVALID_ARG)):
+        ref = (C.cg_chunk_ref * 1)(C.cg_chunk_ref(ct.pointer(cfg.c()), ct.pointer(enc), 1, dst, 100, 50))
+        assert C.lib().cg_decode_chunks_ws_bytes(ref, 1, ct.byref(n)) == want
+    # cg_decode has no host-only control: with every section aligned it would launch
+    assert C.lib().cg_decode(ct.byref(cfg.c()), ct.byref(bad), dst, 0, None) == C.CG_ERR_INVALID_ARG
+    assert C.lib().cg_test_decode_timeout(ct.byref(cfg.c()), ct.byref(bad), dst, 0, None) == C.CG_ERR_INVALID_ARG
+
+
 def test_cache_source_host_checks():
     """cg_cache_source refuses null arguments; without a usable device the
     pointer query itself fails (CUDA error), and nothing is reported usable."""

@@ -175,6 +175,9 @@ def test_corruption_is_flagged_not_faulted():
     e4 = C.Encoded(*[getattr(enc, f).clone() for f in enc.fields()], sizes=enc.sizes)
     e4.payload = e4.payload[: e4.payload.numel() // 2]        # truncated payload section
     cases.append(e4)
+    e5 = C.Encoded(*[getattr(enc, f).clone() for f in enc.fields()], sizes=enc.sizes)
+    e5.table_off[5] += 1                                      # odd table offset: its 16-bit entries unaligned
+    cases.append(e5)
     for i, e in enumerate(cases):
         status = C.new_status()
         C.cg_decode(pc, e, out, status)
