@@ -740,24 +740,30 @@ __device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *et
     const int8_t *ap = a.anchors + (g.chunk_anchor_row0(ch) + (uint64_t)slice * g.apc(ch) + gs / G) * C + c;
     const uint16_t *xp = x + (uint64_t)(c0 + gs) * C;
     const uint8_t *sp = a.sym + ((uint64_t)slice * g.T + c0 + gs) * C + c;
-    uint32_t cur[kV], nxt[kV];
+    uint32_t b0[kV], b1[kV];
     auto load_group = [&](const uint8_t *gp, uint32_t (&buf)[kV]) {
 #pragma unroll
         for (uint32_t i = 0; i < kV; i++) buf[i] = gp[(uint64_t)(i + 1u) * C];
     };
     bool cur_full = kG > 1 && gs >= p0 && gs + G <= p1;
-    if (cur_full) load_group(sp, cur);
-    while (true) {
+    if (cur_full) load_group(sp, b0);
+    // A stream without escapes (the statistics pass counted them per stream)
+    // codes every whole group straight from its symbols; otherwise one vote
+    // per whole group tells whether any of its values escapes.  If none does
+    // (nearly always), its steps skip the escape handling; otherwise -- and
+    // for groups cut by the span -- the values are reloaded, quantized and
+    // coded one by one with it.
+    const bool any_esc = S.e_top != 0;
+    // One group, coded from `cur` when whole, with the next group's symbols
+    // loaded into `nxt`; false once the span's first group is coded.  Two
+    // calls per loop trip swap the buffers' roles instead of copying.
+    auto group = [&](uint32_t (&cur)[kV], uint32_t (&nxt)[kV]) -> bool {
         const bool has_next = gs > p0;
         const uint32_t gn = has_next ? gs - G : 0u;
         const bool nxt_full = kG > 1 && has_next && gn >= p0;
         if (nxt_full) load_group(sp - (uint64_t)G * C, nxt);
-        // One vote per whole group tells whether any of its values escapes.
-        // If none does (nearly always), its steps skip the escape handling;
-        // otherwise -- and for groups cut by the span -- the values are
-        // reloaded, quantized and coded one by one with it.
-        bool fast = false;
-        if (cur_full) {
+        bool fast = cur_full;
+        if (cur_full && any_esc) {
             bool esc = false;
 #pragma unroll
             for (uint32_t i = 0; i < kV; i++) esc = esc || cur[i] == kEsc;
@@ -791,14 +797,15 @@ __device__ __forceinline__ void encode_span(const EncArgs &a, const uint32_t *et
                 }
             }
         }
-        if (!has_next) break;
+        if (!has_next) return false;
         gs = gn;
         xp -= (uint64_t)G * C;
         sp -= (uint64_t)G * C;
         ap -= C;
         cur_full = nxt_full;
-#pragma unroll
-        for (uint32_t i = 0; i < kV; i++) cur[i] = nxt[i];
+        return true;
+    };
+    while (group(b0, b1) && group(b1, b0)) {
     }
     S.top -= 2u * kLanes;
     S.region[S.top + 2u * lane] = (uint16_t)(S.xs >> 16);
