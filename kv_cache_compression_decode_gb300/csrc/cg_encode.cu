@@ -138,10 +138,10 @@ constexpr int kStatsWarps = 16;
 // Every warp takes a contiguous run of tiles and copies them (the block's 32
 // channels: 64 bytes a row) with cp.async into a ring of kStStages
 // shared-memory slots, kStStages - 1 tiles ahead of the one it counts.
-constexpr uint32_t kStSlotRows = 20;
-constexpr uint32_t kStStages = 3;
+constexpr uint32_t kStSlotRows = 30;
+constexpr uint32_t kStStages = 2;
 constexpr uint32_t kStRowBytes = kLanes * 2u;
-constexpr uint32_t kStSlotBytes = kStSlotRows * kStRowBytes;              // 1280 B
+constexpr uint32_t kStSlotBytes = kStSlotRows * kStRowBytes;              // 1920 B
 constexpr uint32_t kStRingBytes = kStatsWarps * kStStages * kStSlotBytes;  // 60 KB
 constexpr uint32_t kE1Batch = 8;  // 16-byte anchor-row loads in flight per lane
 
@@ -398,9 +398,9 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
             ach = ch;
             abase = g.chunk_anchor_row0(ch) + (uint64_t)slice * g.apc(ch);
         }
-        if (G == 10 && n == 20) {  // the common tile: two whole 10-token groups
+        if (G == 10 && n == kStSlotRows) {  // the common tile: three whole 10-token groups
 #pragma unroll
-            for (uint32_t h = 0; h < 2; h++) {
+            for (uint32_t h = 0; h < kStSlotRows / 10u; h++) {
                 const uint16_t *gr = rows + h * 10u * kLanes;
                 const float v0 = h2f(gr[0]);
                 nan_acc = __fmaf_rn(v0, 0.f, nan_acc);
