@@ -382,10 +382,14 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
     uint64_t abase = 0;          // anchor row of group 0 of chunk ach
     float xa = gpos0 ? __fmul_rn(anchor_q(h2f(a_raw), inv_sa), sa) : 0.f;
     float nan_acc = 0.f;
+    // tiles are consecutive in token order: each starts where the one before ends
+    uint32_t t0_in = in.ch * g.chunk + in.first(R);
+    uint8_t *spt = lv.sym + ((uint64_t)slice * g.T + cur.ch * g.chunk + cur.first(R)) * (kC ? kC : g.C) + c;
     for (uint32_t t = 0; t < nt; t++) {
         if (t + kStStages - 1u < nt) {
-            stage_tile(ring_s + ((t + kStStages - 1u) % kStStages) * kStSlotBytes, xl, g.C, C8,
-                       in.ch * g.chunk + in.first(R), in.rows(R), lane);
+            const uint32_t rr = in.rows(R);
+            stage_tile(ring_s + ((t + kStStages - 1u) % kStStages) * kStSlotBytes, xl, g.C, C8, t0_in, rr, lane);
+            t0_in += rr;
             in.next(g, R);
         }
         cp_async_commit();
@@ -393,7 +397,6 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
         __syncwarp();
         const uint16_t *rows = reinterpret_cast<const uint16_t *>(ring + (t % kStStages) * kStSlotBytes) + lane;
         const uint32_t ch = cur.ch, p = cur.first(R), n = cur.rows(R);
-        uint8_t *spt = lv.sym + ((uint64_t)slice * g.T + ch * g.chunk + p) * (kC ? kC : g.C) + c;  // row 0 of the tile
         if (ch != ach) {
             ach = ch;
             abase = g.chunk_anchor_row0(ch) + (uint64_t)slice * g.apc(ch);
@@ -439,6 +442,7 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
                 }
             }
         }
+        spt += (uint64_t)n * (kC ? kC : g.C);
         cur.next(g, R);
         __syncwarp();  // the slot is read by every lane before it is refilled
     }
