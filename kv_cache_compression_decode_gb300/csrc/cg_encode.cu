@@ -454,10 +454,19 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
             lv.raw_delta[((uint64_t)slice * g.C + grp * kLanes + (i & 31u)) * 256u + (i >> 5)] = hist[i];
 
     // E5: normalize each channel's counts to a 16-bit table (warp per
-    // (level, channel)).
-    for (uint32_t jj = warp; jj < NL * kLanes; jj += kStatsWarps) {
-        const uint32_t lvl = jj / kLanes, j = jj % kLanes;
-        const uint32_t *hl = hist + lvl * 256u * kLanes;
+    // (level, channel)).  A level's [symbol][channel] counts are first
+    // copied channel-major into the staging ring, which is free by now, with
+    // rows of 257 words: a channel's 256 counts are then spread over all
+    // banks, where in place they all sit in one.
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    uint32_t *histT = reinterpret_cast<uint32_t *>(hist + NL * 256u * kLanes);
+    static_assert(kLanes * 257u * 4u <= kStRingBytes, "transposed counts fit the ring");
+    for (uint32_t lvl = 0; lvl < NL; lvl++) {
+      __syncthreads();
+      for (uint32_t s = warp; s < 256u; s += kStatsWarps) histT[lane * 257u + s] = hist[(lvl * 256u + s) * kLanes + lane];
+      __syncthreads();
+      for (uint32_t j = warp; j < kLanes; j += kStatsWarps) {
+        const uint32_t *hl = histT + j * 257u;
         uint16_t *ftab = lv.ftab[lvl];
         uint32_t *tlohi = lv.tlohi[lvl], *twidth = lv.twidth[lvl];
         const uint64_t table = (uint64_t)slice * g.C + grp * kLanes + j;
@@ -467,7 +476,7 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
         #pragma unroll
         for (int i = 0; i < 8; i++) {
             uint32_t s = (uint32_t)i * 32u + lane;
-            n[i] = hl[s * kLanes + j];
+            n[i] = hl[s];
             N += n[i];
             if (n[i]) {
                 lo = min(lo, s);
@@ -539,6 +548,7 @@ __global__ void __launch_bounds__(kStatsWarps * 32, NL == 1 ? 2 : 1) k_stats(Enc
             tlohi[table] = lo | (hi << 8);
             twidth[table] = 2u + 2u * (hi - lo + 1u);
         }
+      }
     }
 }
 
