@@ -888,6 +888,27 @@ __global__ void __launch_bounds__(kMaxEncWarps * 32, 3) k_encode(EncArgs a, Step
     }
 }
 
+// Copy of one stream's words, which end at the end of its 16-byte aligned
+// scratch region and so start m words (m = 2 K or 2 K + 1) past a 16-byte
+// boundary: output piece j (16 bytes) takes the aligned source pieces j and
+// j + 1 and shifts them down by m words -- K whole 32-bit words picked at
+// compile time, then 16 bits by a funnel shift when m is odd.  Piece j + 1
+// is read only while it starts inside the stream's words (else zero), so
+// nothing past the region is read and the words past the stream, which the
+// payload pads with zeros, come out as zeros.
+template <uint32_t K>
+__device__ __forceinline__ void pack_stream(const uint4 *src, uint4 *dst, uint64_t n16, uint64_t a0, uint64_t wend,
+                                            uint32_t m, uint32_t lane) {
+    const uint32_t sh = (m & 1u) * 16u;
+    for (uint64_t j = lane; j < n16; j += 32) {
+        const uint4 x = src[j];
+        const uint4 y = m && a0 + 8u * j + 8u < wend ? src[j + 1] : make_uint4(0, 0, 0, 0);
+        const uint32_t r[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+        dst[j] = make_uint4(__funnelshift_r(r[K], r[K + 1], sh), __funnelshift_r(r[K + 1], r[K + 2], sh),
+                            __funnelshift_r(r[K + 2], r[K + 3], sh), __funnelshift_r(r[K + 3], r[K + 4], sh));
+    }
+}
+
 __global__ void __launch_bounds__(256) k_pack(EncArgs a) {
     const uint64_t k = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint32_t lane = threadIdx.x & 31u;
@@ -895,19 +916,20 @@ __global__ void __launch_bounds__(256) k_pack(EncArgs a) {
     const uint32_t cnt = a.words_count[k];
     const uint64_t off = a.stream_off[k], end = a.stream_off[k + 1];
     if (end > a.payload_cap) return;  // RANGE already flagged by the scan
-    // 16 bytes (8 words) per lane and pass: eight independent 2-byte loads
-    // (the words start at any 2-byte boundary of the scratch region), one
-    // 16-byte store (stream offsets and the payload are 16-byte aligned);
-    // words past the stream are the zero padding
-    const uint16_t *src = a.scratch + k * a.region_words + (a.region_words - cnt);
+    // the stream's words: [w0, wend) of the scratch buffer, wend = the end of
+    // its region (a multiple of 8 words); stream offsets and the payload are
+    // 16-byte aligned, and the stream takes ceil(cnt / 8) pieces of it
+    const uint64_t wend = (k + 1u) * a.region_words, w0 = wend - cnt;
+    const uint32_t m = (uint32_t)(w0 & 7u);
+    const uint64_t a0 = w0 - m;
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.scratch + a0);
     uint4 *dst = reinterpret_cast<uint4 *>(a.payload + off);
     const uint64_t n16 = (end - off) >> 4;
-    for (uint64_t j = lane; j < n16; j += 32) {
-        const uint64_t i0 = j * 8u;
-        uint32_t w[8];
-#pragma unroll
-        for (uint32_t i = 0; i < 8; i++) w[i] = i0 + i < cnt ? src[i0 + i] : 0u;
-        dst[j] = make_uint4(w[0] | w[1] << 16, w[2] | w[3] << 16, w[4] | w[5] << 16, w[6] | w[7] << 16);
+    switch (m >> 1) {
+        case 0: pack_stream<0>(src, dst, n16, a0, wend, m, lane); break;
+        case 1: pack_stream<1>(src, dst, n16, a0, wend, m, lane); break;
+        case 2: pack_stream<2>(src, dst, n16, a0, wend, m, lane); break;
+        default: pack_stream<3>(src, dst, n16, a0, wend, m, lane); break;
     }
 }
 
