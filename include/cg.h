@@ -285,10 +285,10 @@ cg_status cg_decode_chunks(const cg_chunk_ref *refs, uint32_t n, void *ws, size_
  * process exits.  It calls no cudaMalloc or cudaFree and no allocating
  * routine; the host side plans into static storage as well.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) and keeps it for the life of the process; make
- *     that first call before any stream capture.  The kept address belongs
- *     to the device's primary context: after cudaDeviceReset on that device
- *     the library must be loaded again before this call is used.
+ *     (cudaGetSymbolAddress) and keeps it for the life of the process.  The
+ *     kept address belongs to the device's primary context: after
+ *     cudaDeviceReset on that device the library must be loaded again before
+ *     this call is used.
  *   - Every call rewrites the array, so calls that overlap on the GPU race:
  *     issue them on one stream, or order them with events.  Calls from
  *     several host threads are serialized by a lock.
