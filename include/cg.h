@@ -39,10 +39,12 @@
  *     (1u << code): CG_ERR_NONFINITE, CG_ERR_RANGE, CG_ERR_CORRUPT,
  *     CG_ERR_TIMEOUT.  Read it after synchronizing; cg_status_from_flags()
  *     turns it into a status.  Outputs are undefined when it is non-zero.
- *     Bits 16..22 say which check failed (diagnostics only): 16 malformed
+ *     Bits 16..23 say which check failed (diagnostics only): 16 malformed
  *     table, 17 stream/escape offsets out of range, 18 coder end state,
  *     19 stream length, 20 non-zero padding, 21 escape count, 22 a bounded
- *     device wait gave up.
+ *     device wait gave up, 23 a decode block's shared memory was not placed
+ *     where the decoder's layout needs it (reported with CG_ERR_CUDA; the
+ *     block writes nothing).
  *   - fp16 tensors are passed as their 16-bit patterns (uint16_t).
  *
  * Encoded object (all sections little-endian; per-chunk sections are

@@ -91,16 +91,50 @@ constexpr uint32_t kTestSpinLimit = 16;
 static_assert(kLanes * kMaxRun <= (kRingSegs - kAhead - 1) * kSegWords + 1, "ring window");
 static_assert((kRingSegs & (kRingSegs - 1u)) == 0, "slot = segment & (kRingSegs - 1)");
 
-// Dynamic shared memory layout of a decode block.
-constexpr uint32_t kTabOff = 0;                              // u32 [256][32]: c | (f - 1) << 16
-constexpr uint32_t kCoarseOff = kTabOff + 256 * kLanes * 4;  // u16 [256][32]: s0 << 8 | d (see top)
-constexpr uint32_t kDqOff = kCoarseOff + 256 * kLanes * 2;   // f32 [256]: float(s - 127) * step
-constexpr uint32_t kHiOff = kDqOff + 256 * 4;                // u32 [32]: lo << 16 | hi
-constexpr uint32_t kScaleOff = kHiOff + kLanes * 4;          // f32 [32]
-constexpr uint32_t kBadOff = kScaleOff + kLanes * 4;         // int
-constexpr uint32_t kBarOff = kBadOff + 16;                   // u64 [warps][kRingSegs]
-__host__ __device__ constexpr uint32_t ring_off(uint32_t nwarps) { return kBarOff + nwarps * kRingSegs * 8; }
-__host__ __device__ constexpr uint32_t dec_smem_bytes(uint32_t nwarps) { return ring_off(nwarps) + nwarps * kRingWords * 2; }
+// Dynamic shared memory of a decode block of nw warps.  Every warp's ring
+// starts on a 2048-byte boundary of the shared window, so that the
+// renormalization forms a word's address as ring | offset.  Dynamic shared
+// memory begins either on such a boundary or 1024 bytes past one; the
+// dequant table (1 KB) goes after the rings in the first case and before
+// them in the second, and the rest follows both at fixed offsets from the
+// tables base tb = nw * kRingBytes + 1024:
+//   rings u16 [nw][1024], dq f32 [256]   or   dq f32 [256], rings u16 [nw][1024]
+//   tb + kTabOff     u32 [256][32]: c | (f - 1) << 16
+//   tb + kCoarseOff  u16 [256][32]: s0 << 8 | d (see top)
+//   tb + kHiOff      u32 [32]: lo << 16 | hi
+//   tb + kScaleOff   f32 [32]
+//   tb + kBadOff     int
+//   tb + kBarOff     u64 [nw][kRingSegs]
+constexpr uint32_t kRingBytes = kRingWords * 2;               // 2048
+constexpr uint32_t kDqBytes = 256 * 4;
+constexpr uint32_t kTabOff = 0;
+constexpr uint32_t kCoarseOff = kTabOff + 256 * kLanes * 4;
+constexpr uint32_t kHiOff = kCoarseOff + 256 * kLanes * 2;
+constexpr uint32_t kScaleOff = kHiOff + kLanes * 4;
+constexpr uint32_t kBadOff = kScaleOff + kLanes * 4;
+constexpr uint32_t kBarOff = kBadOff + 16;
+static_assert(kRingBytes == 2048u && kDqBytes == 1024u, "ring alignment and the dequant table's kilobyte");
+__host__ __device__ constexpr uint32_t dec_smem_bytes(uint32_t nwarps) {
+    return nwarps * kRingBytes + kDqBytes + kBarOff + nwarps * kRingSegs * 8;
+}
+
+// A block's pieces of that layout.
+struct Shm {
+    uint8_t *tb;  // tables base
+    float *dq;
+    uint16_t *ring;  // warp 0's ring; warp w's at ring + w * kRingWords
+};
+
+// False (for the whole block) when dynamic shared memory does not start on
+// or 1024 bytes past a 2048-byte boundary, which the layout needs.
+__device__ __forceinline__ bool shm_layout(uint8_t *smem, uint32_t nw, Shm &S) {
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem);
+    const bool odd = (base & 1024u) != 0;
+    S.tb = smem + nw * kRingBytes + kDqBytes;
+    S.dq = reinterpret_cast<float *>(odd ? smem : smem + nw * kRingBytes);
+    S.ring = reinterpret_cast<uint16_t *>(odd ? smem + kDqBytes : smem);
+    return (base & 1023u) == 0;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -216,13 +250,13 @@ __device__ __forceinline__ bool table_span(const DecObj &o, uint64_t table, uint
 }
 
 __device__ __forceinline__ bool prepare_tables(const DecObj &o, uint32_t slice, uint32_t grp, float step,
-                                               uint8_t *smem, uint32_t *status) {
+                                               const Shm &S, uint32_t *status) {
+    uint8_t *const smem = S.tb;
     const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const uint64_t table = (uint64_t)slice * o.g.C + grp * kLanes + lane;
     uint32_t *tab = reinterpret_cast<uint32_t *>(smem + kTabOff) + lane;
     uint32_t *part = reinterpret_cast<uint32_t *>(smem + kCoarseOff) + lane;  // [kBatches][32] scratch
-    float *dq = reinterpret_cast<float *>(smem + kDqOff);
-    for (uint32_t s = threadIdx.x; s < 256u; s += blockDim.x) dq[s] = __fmul_rn(__int2float_rn((int)s - 127), step);
+    for (uint32_t s = threadIdx.x; s < 256u; s += blockDim.x) S.dq[s] = __fmul_rn(__int2float_rn((int)s - 127), step);
 
     // phase 1
     uint64_t at;
@@ -360,9 +394,11 @@ __device__ __forceinline__ float lds_f32(uint32_t a) {
 // state fell below 2^16 take the next words of the stream in lane order.
 // Written in PTX so that the state takes its word under the predicate
 // (x = (x << 16) | w for the lanes that need one) instead of a select; the
-// ring load is unconditional and its index wraps within the ring.
+// ring load is unconditional.  pb counts the stream bytes taken; the ring
+// starts on a 2048-byte boundary, so a word's address is ring | (byte
+// offset mod 2048).
 static_assert(kStateLow == 65536u && kRingWords == 1024u, "renorm constants");
-__device__ __forceinline__ void renorm(uint32_t &x, uint32_t xn, uint32_t &pw, const Lut &T, const uint16_t *ring) {
+__device__ __forceinline__ void renorm(uint32_t &x, uint32_t xn, uint32_t &pb, const Lut &T, const uint16_t *ring) {
     const uint32_t rs = (uint32_t)__cvta_generic_to_shared(ring);
     x = xn;
     asm("{\n\t.reg .pred p;\n\t.reg .b32 b, t, i, w;\n\t"
@@ -370,24 +406,24 @@ __device__ __forceinline__ void renorm(uint32_t &x, uint32_t xn, uint32_t &pw, c
         "vote.sync.ballot.b32 b, p, 0xffffffff;\n\t"
         "and.b32 t, b, %2;\n\t"                     // needing lanes below this one
         "popc.b32 t, t;\n\t"
-        "add.u32 i, %1, t;\n\t"
-        "and.b32 i, i, 1023;\n\t"                   // ring index
-        "mad.lo.u32 i, i, 2, %3;\n\t"
+        "mad.lo.u32 i, t, 2, %1;\n\t"               // the lane's word: stream byte offset
+        "and.b32 i, i, 2047;\n\t"
+        "or.b32 i, i, %3;\n\t"                      // ... in the ring
         "ld.shared.u16 w, [i];\n\t"
         "@p mad.lo.u32 %0, %0, 65536, w;\n\t"       // (x << 16) | w
         "popc.b32 t, b;\n\t"
-        "add.u32 %1, %1, t;\n\t}"                   // words taken by the warp
-        : "+r"(x), "+r"(pw)
+        "mad.lo.u32 %1, t, 2, %1;\n\t}"             // bytes taken by the warp
+        : "+r"(x), "+r"(pb)
         : "r"(T.lt), "r"(rs)
         : "memory");
 }
 
 // State update for the lane's symbol (r = slot - c_s, fm1 = f_s - 1, a
 // form that also holds for f = 65536) and renormalization.
-__device__ __forceinline__ void update(uint32_t &x, uint32_t &pw, const Lut &T, const uint16_t *ring, uint32_t r,
+__device__ __forceinline__ void update(uint32_t &x, uint32_t &pb, const Lut &T, const uint16_t *ring, uint32_t r,
                                        uint32_t fm1) {
     const uint32_t xh = x >> 16;
-    renorm(x, xh * fm1 + xh + r, pw, T, ring);
+    renorm(x, xh * fm1 + xh + r, pb, T, ring);
 }
 
 __device__ __forceinline__ uint16_t to_half(float v) { return __half_as_ushort(__float2half_rn(v)); }
@@ -399,7 +435,7 @@ __device__ __forceinline__ uint16_t to_half(float v) { return __half_as_ushort(_
 // both, and that path walks with a uniform loop so the common path carries
 // no divergence bookkeeping.
 template <bool kHasEsc>
-__device__ __forceinline__ float rans_step(uint32_t &x, uint32_t &pw, const Lut &T, const uint16_t *ring, float step,
+__device__ __forceinline__ float rans_step(uint32_t &x, uint32_t &pb, const Lut &T, const uint16_t *ring, float step,
                                            const int32_t *escapes, uint32_t &ep, uint32_t ee) {
     const uint32_t e0 = T.coarse[((x >> 8) & 0xFFu) * kLanes];
     uint32_t s = (e0 + (x & 0xFFu)) >> 8;
@@ -430,7 +466,7 @@ __device__ __forceinline__ float rans_step(uint32_t &x, uint32_t &pw, const Lut 
     } else {
         dq = T.dq[s];
     }
-    update(x, pw, T, ring, r, fm1);
+    update(x, pb, T, ring, r, fm1);
     return dq;
 }
 
@@ -498,7 +534,7 @@ struct PagedOut {
 // kG = 10 / kC = 1024 select compile-time group size / row stride (0: runtime).
 template <bool kHasEsc, uint32_t kG, uint32_t kC, class Out, bool kW>
 __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice, uint32_t grp, uint32_t sp,
-                                                 float step, const uint8_t *smem, Ring &R, Out O, uint32_t *status,
+                                                 float step, const Shm &S, Ring &R, Out O, uint32_t *status,
                                                  uint64_t sb, uint64_t se, uint32_t eb, uint32_t ee,
                                                  uint32_t nsteps) {
     const Geom &g = o.g;
@@ -507,10 +543,10 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
     Lut T;
     T.lane = threadIdx.x & 31u;
     T.lt = lanemask_lt();
-    T.tab = reinterpret_cast<const uint32_t *>(smem + kTabOff) + T.lane;
-    T.coarse = reinterpret_cast<const uint16_t *>(smem + kCoarseOff) + T.lane;
-    T.dq = reinterpret_cast<const float *>(smem + kDqOff);
-    T.hi = reinterpret_cast<const uint32_t *>(smem + kHiOff)[T.lane] & 0xFFFFu;
+    T.tab = reinterpret_cast<const uint32_t *>(S.tb + kTabOff) + T.lane;
+    T.coarse = reinterpret_cast<const uint16_t *>(S.tb + kCoarseOff) + T.lane;
+    T.dq = S.dq;
+    T.hi = reinterpret_cast<const uint32_t *>(S.tb + kHiOff)[T.lane] & 0xFFFFu;
     T.tab_s = smem_addr(T.tab);
     T.coarse_s = smem_addr(T.coarse);
     T.dq_s = smem_addr(T.dq);
@@ -518,7 +554,7 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
     const uint32_t ch = sp / g.spans_full, span = sp - ch * g.spans_full;
     const uint32_t c0 = ch * g.chunk, len = g.chunk_len(ch);
     const uint32_t p0 = span * g.tps, p1 = min(p0 + g.tps, len);
-    const float sa = reinterpret_cast<const float *>(smem + kScaleOff)[T.lane];
+    const float sa = reinterpret_cast<const float *>(S.tb + kScaleOff)[T.lane];
     const uint16_t *ring = R.buf;
 
     Cursor K;
@@ -529,12 +565,12 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
     K.wseg = 0;
     K.avail = 0;
     K.alive = true;
-    uint32_t x = 0, pw = 0, ep = eb;
+    uint32_t x = 0, pb = 0, ep = eb;  // pb: stream bytes taken (words: pb / 2)
     if (nsteps) {
         for (uint32_t k = 0; k < kAhead; k++) ring_issue<kW>(R, K, k);
         ensure<kW>(R, K, 2u * kLanes);
         x = ((uint32_t)ring[2 * T.lane] << 16) | ring[2 * T.lane + 1];
-        pw = 2u * kLanes;
+        pb = 4u * kLanes;
     }
 
     uint32_t p = p0;
@@ -545,8 +581,8 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
     if (gp0) {  // head: the rest of a group whose anchor lies before the span
         const uint32_t cnt = min(G - gp0, p1 - p);
         for (uint32_t k = 0; k < cnt && K.alive && O.ok(); k++) {
-            if (k % kMaxRun == 0) ensure<kW>(R, K, pw + kLanes * min(kMaxRun, cnt - k));
-            *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
+            if (k % kMaxRun == 0) ensure<kW>(R, K, (pb >> 1) + kLanes * min(kMaxRun, cnt - k));
+            *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pb, T, ring, step, o.escapes, ep, ee)));
         }
         p += cnt;
         O.advance(cnt, C);
@@ -558,7 +594,7 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
         xa = __fmul_rn((float)qa_next, sa);
         if (p + G < p1) qa_next = arow[C];  // prefetch the next group's anchor
         *O.row(0, C) = to_half(xa);
-        if (kG) ensure<kW>(R, K, pw + kLanes * (kG - 1u));  // kG - 1 <= kMaxRun
+        if (kG) ensure<kW>(R, K, (pb >> 1) + kLanes * (kG - 1u));  // kG - 1 <= kMaxRun
         if constexpr (kG == 10) {
             // The nine delta steps written out.  Per step: the bucket lookup,
             // then one vote for the rare cases -- a slot past the end of the
@@ -590,7 +626,7 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
             }                                                                                               \
             dq = lds_f32(T.dq_s + s * 4u);                                                                  \
         }                                                                                                   \
-        update(x, pw, T, ring, r, fm1);                                                                     \
+        update(x, pb, T, ring, r, fm1);                                                                     \
         *O.row(K, C) = to_half(__fadd_rn(xa, dq));                                                          \
     }
             CG_STEP(1) CG_STEP(2) CG_STEP(3) CG_STEP(4) CG_STEP(5) CG_STEP(6) CG_STEP(7) CG_STEP(8) CG_STEP(9)
@@ -599,12 +635,12 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
         cg_slow:
 #pragma unroll 1
             for (; k < kG; k++)
-                *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
+                *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pb, T, ring, step, o.escapes, ep, ee)));
         cg_done:;
         } else {
             for (uint32_t k = 1; k < G; k++) {
-                if ((k - 1u) % kMaxRun == 0) ensure<kW>(R, K, pw + kLanes * min(kMaxRun, G - k));
-                *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
+                if ((k - 1u) % kMaxRun == 0) ensure<kW>(R, K, (pb >> 1) + kLanes * min(kMaxRun, G - k));
+                *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pb, T, ring, step, o.escapes, ep, ee)));
             }
         }
         p += G;
@@ -616,8 +652,8 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
         *O.row(0, C) = to_half(xa);
         const uint32_t cnt = p1 - p - 1u;
         for (uint32_t k = 1; k <= cnt && K.alive; k++) {
-            if ((k - 1u) % kMaxRun == 0) ensure<kW>(R, K, pw + kLanes * min(kMaxRun, cnt - k + 1u));
-            *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pw, T, ring, step, o.escapes, ep, ee)));
+            if ((k - 1u) % kMaxRun == 0) ensure<kW>(R, K, (pb >> 1) + kLanes * min(kMaxRun, cnt - k + 1u));
+            *O.row(k, C) = to_half(__fadd_rn(xa, rans_step<kHasEsc>(x, pb, T, ring, step, o.escapes, ep, ee)));
         }
     }
     // drain the copies still in flight (also after a wait gave up) before the
@@ -632,6 +668,7 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
         return true;
     }
     uint32_t why = ep == ee ? 0u : kWhyEscapes;
+    const uint32_t pw = pb >> 1;  // words taken
     if (nsteps) {
         if (!__all_sync(kFull, x == kStateLow)) why |= kWhyState;
         if (!(pw <= K.nw && K.nw - pw < 8u)) why |= kWhyLength;
@@ -649,7 +686,7 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
 // further stream.
 template <class Out, bool kW = false>
 __device__ bool decode_span(const DecObj &o, uint32_t slice, uint32_t grp, uint32_t sp, float step,
-                            const uint8_t *smem, Ring &R, Out O, uint32_t *status) {
+                            const Shm &S, Ring &R, Out O, uint32_t *status) {
     const Geom &g = o.g;
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t ch = sp / g.spans_full, span = sp - ch * g.spans_full;
@@ -667,19 +704,19 @@ __device__ bool decode_span(const DecObj &o, uint32_t slice, uint32_t grp, uint3
         return true;
     }
 #define CG_SPAN(E, GG, CC) \
-    decode_span_impl<E, GG, CC, Out, kW>(o, slice, grp, sp, step, smem, R, O, status, sb, se, eb, ee, nsteps)
+    decode_span_impl<E, GG, CC, Out, kW>(o, slice, grp, sp, step, S, R, O, status, sb, se, eb, ee, nsteps)
     if (g.G == 10 && g.C == 1024) return ee != eb ? CG_SPAN(true, 10, 1024) : CG_SPAN(false, 10, 1024);
     if (g.G == 10) return ee != eb ? CG_SPAN(true, 10, 0) : CG_SPAN(false, 10, 0);
     return ee != eb ? CG_SPAN(true, 0, 0) : CG_SPAN(false, 0, 0);
 #undef CG_SPAN
 }
 
-__device__ __forceinline__ Ring make_ring(uint8_t *smem, uint32_t nwarps) {
+__device__ __forceinline__ Ring make_ring(const Shm &S) {
     const uint32_t warp = threadIdx.x >> 5;
     Ring R;
-    R.buf = reinterpret_cast<const uint16_t *>(smem + ring_off(nwarps)) + warp * kRingWords;
+    R.buf = S.ring + warp * kRingWords;
     R.buf_s = smem_addr(R.buf);
-    R.bar_s = smem_addr(smem + kBarOff) + warp * kRingSegs * 8u;
+    R.bar_s = smem_addr(S.tb + kBarOff) + warp * kRingSegs * 8u;
     R.phase = 0;
     if ((threadIdx.x & 31u) == 0) {
         for (uint32_t k = 0; k < kRingSegs; k++) mbar_init(R.bar_s + 8u * k);
@@ -699,8 +736,13 @@ __global__ void __maxnreg__(kDecRegs) k_decode_all(DecObj o, StepTable st, uint1
     const uint32_t grp = blockIdx.x, slice = blockIdx.y, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const uint32_t c = grp * kLanes + (threadIdx.x & 31u);
     const float step = st.v[slice >> 1];
-    Ring R = make_ring(smem, nw);
-    if (!prepare_tables(o, slice, grp, step, smem, status)) return;
+    Shm S;
+    if (!shm_layout(smem, nw, S)) {
+        if (threadIdx.x == 0) flag_why(status, CG_ERR_CUDA, kWhyLayout);
+        return;
+    }
+    Ring R = make_ring(S);
+    if (!prepare_tables(o, slice, grp, step, S, status)) return;
     for (uint64_t sp = warp; sp < o.g.spans_total; sp += nw) {
         bool alive;
         if (kPaged) {
@@ -713,10 +755,10 @@ __global__ void __maxnreg__(kDecRegs) k_decode_all(DecObj o, StepTable st, uint1
             O.block_stride = pd.block_stride;
             O.ts = pd.token_stride;
             O.good = true;
-            alive = decode_span<PagedOut, kW>(o, slice, grp, (uint32_t)sp, step, smem, R, O, status);
+            alive = decode_span<PagedOut, kW>(o, slice, grp, (uint32_t)sp, step, S, R, O, status);
         } else {
             const LinearOut<false> O{out + (uint64_t)slice * o.g.T * o.g.C, 0, c, nullptr};
-            alive = decode_span<LinearOut<false>, kW>(o, slice, grp, (uint32_t)sp, step, smem, R, O, status);
+            alive = decode_span<LinearOut<false>, kW>(o, slice, grp, (uint32_t)sp, step, S, R, O, status);
         }
         if (!alive) break;
     }
@@ -730,14 +772,19 @@ __global__ void __maxnreg__(kDecRegs) k_decode_jobs(const DecObj *objs, const De
     const DecObj &o = objs[job.obj];
     const uint32_t warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const float step = o.step[job.slice >> 1];
-    Ring R = make_ring(smem, nw);
-    if (!prepare_tables(o, job.slice, job.grp, step, smem, status)) return;
+    Shm S;
+    if (!shm_layout(smem, nw, S)) {
+        if (threadIdx.x == 0) flag_why(status, CG_ERR_CUDA, kWhyLayout);
+        return;
+    }
+    Ring R = make_ring(S);
+    if (!prepare_tables(o, job.slice, job.grp, step, S, status)) return;
     for (uint32_t i = warp; i < job.span_count; i += nw) {
         const SpanRef sr = spans[job.span_begin + i];
         const RefDst rd = refs[sr.ref];
         const LinearOut<true> O{rd.dst + (uint64_t)job.slice * rd.dst_tokens * o.g.C, rd.shift,
                                 job.grp * kLanes + (threadIdx.x & 31u), nullptr};
-        if (!decode_span(o, job.slice, job.grp, sr.span, step, smem, R, O, status)) break;
+        if (!decode_span(o, job.slice, job.grp, sr.span, step, S, R, O, status)) break;
     }
 }
 

@@ -96,6 +96,7 @@ constexpr uint32_t kWhyLength = 1u << 19;   // words consumed do not match the s
 constexpr uint32_t kWhyPadding = 1u << 20;  // non-zero padding after the stream
 constexpr uint32_t kWhyEscapes = 1u << 21;  // escapes consumed do not match the count
 constexpr uint32_t kWhyWait = 1u << 22;     // a bounded wait gave up
+constexpr uint32_t kWhyLayout = 1u << 23;   // a decode block's shared memory was not placed as its layout needs
 
 __device__ inline void flag_why(uint32_t *status, cg_status code, uint32_t why) {
     if (status) atomicOr(status, (1u << (uint32_t)code) | why);
