@@ -1,17 +1,19 @@
 // cg_decode.cu -- GPU decoder of the KV-cache codec (sm_103a).
 //
-// One thread block per (object, layer, K/V, 32-channel group).  Warp 0 turns
-// the block's 32 compact frequency tables into shared-memory symbol tables,
-// then every warp fills a share of the bucket table; both are laid out
-// [entry][lane]:
+// One thread block per (object, layer, K/V, 32-channel group).  The block's
+// warps turn its 32 compact frequency tables into shared-memory symbol
+// tables and a bucket table, both laid out [entry][lane]:
 //   tab    [256][32] u32   c_s | (f_s - 1) << 16 (f - 1 keeps f = 65536, a
 //                          single-symbol table, within 16 bits)
-//   coarse [256][32] u16   bucket b (slots 256 b .. 256 b + 255): s0 << 8 | d,
-//                          s0 the symbol holding slot 256 b, d = 256 (b + 1) -
-//                          (end of s0) when s0 ends inside the bucket, else 0
+//   coarse [256][32] u16   bucket b (slots 256 b .. 256 b + 255):
+//                          (s0 << 8 | d) - 256 b mod 2^16, s0 the symbol
+//                          holding slot 256 b, d = 256 (b + 1) - (end of s0)
+//                          when s0 ends inside the bucket, else 0
 // Then every warp decodes whole streams (lane = channel): per step the lane
-// finds its symbol as (coarse + (slot & 255)) >> 8 -- the carry out of the low
-// byte steps past s0 exactly when the slot lies beyond s0's end -- takes one
+// finds its symbol as byte 1 of coarse + x (x the 32-bit state, whose low 16
+// bits are the slot): that sum is (s0 << 8 | d) + (slot & 255) plus a
+// multiple of 2^16, and the carry out of its low byte steps past s0 exactly
+// when the slot lies beyond s0's end.  The lane then takes one
 // more symbol in the rare bucket that holds a second end before the slot, and
 // walks on only with three or more (each a few lane-steps in a thousand); it then
 // updates its 32-bit range-ANS state, and the warp
@@ -100,7 +102,7 @@ static_assert((kRingSegs & (kRingSegs - 1u)) == 0, "slot = segment & (kRingSegs 
 // tables base tb = nw * kRingBytes + 1024:
 //   rings u16 [nw][1024], dq f32 [256]   or   dq f32 [256], rings u16 [nw][1024]
 //   tb + kTabOff     u32 [256][32]: c | (f - 1) << 16
-//   tb + kCoarseOff  u16 [256][32]: s0 << 8 | d (see top)
+//   tb + kCoarseOff  u16 [256][32]: (s0 << 8 | d) - 256 b (see top)
 //   tb + kHiOff      u32 [32]: lo << 16 | hi
 //   tb + kScaleOff   f32 [32]
 //   tb + kBadOff     int
@@ -326,11 +328,13 @@ __device__ __forceinline__ bool prepare_tables(const DecObj &o, uint32_t slice, 
     __syncthreads();
     if (*reinterpret_cast<const int *>(smem + kBadOff)) return false;
 
-    // phase 3: bucket b (slots 256 b .. 256 b + 255) holds s0 << 8 | d, s0
-    // the symbol containing slot 256 b -- the largest s in [lo, hi] with
-    // c_s <= 256 b, found by a fixed 8-step binary search over the lane's
-    // symbol table -- and d = 256 (b + 1) - (end of s0) when s0 ends inside
-    // the bucket, else 0.  Four searches run side by side.
+    // phase 3: bucket b (slots 256 b .. 256 b + 255) holds (s0 << 8 | d) -
+    // 256 b mod 2^16, s0 the symbol containing slot 256 b -- the largest s in
+    // [lo, hi] with c_s <= 256 b, found by a fixed 8-step binary search over
+    // the lane's symbol table -- and d = 256 (b + 1) - (end of s0) when s0
+    // ends inside the bucket, else 0.  (s0 << 8 | d) + (slot & 255) stays
+    // below 2^16: only symbol 255 could carry past it, and it ends at 2^16.
+    // Four searches run side by side.
     {
         constexpr uint32_t kU = 4;
         const uint32_t lh = reinterpret_cast<const uint32_t *>(smem + kHiOff)[lane];
@@ -354,7 +358,7 @@ __device__ __forceinline__ bool prepare_tables(const DecObj &o, uint32_t slice, 
                 if (b < 256u) {
                     const uint32_t e = tab[sym[u] * kLanes];
                     const uint32_t end = (e & 0xFFFFu) + (e >> 16) + 1u, bend = b * 256u + 256u;
-                    coarse[b * kLanes] = (uint16_t)(sym[u] << 8 | (end < bend ? bend - end : 0u));
+                    coarse[b * kLanes] = (uint16_t)((sym[u] << 8 | (end < bend ? bend - end : 0u)) - (b << 8));
                 }
             }
         }
@@ -438,7 +442,7 @@ template <bool kHasEsc>
 __device__ __forceinline__ float rans_step(uint32_t &x, uint32_t &pb, const Lut &T, const uint16_t *ring, float step,
                                            const int32_t *escapes, uint32_t &ep, uint32_t ee) {
     const uint32_t e0 = T.coarse[((x >> 8) & 0xFFu) * kLanes];
-    uint32_t s = (e0 + (x & 0xFFu)) >> 8;
+    uint32_t s = __byte_perm(e0 + x, 0, 0x4441);
     uint32_t e = T.tab[s * kLanes];
     uint32_t r = (x - e) & 0xFFFFu;  // slot - c_s: the slot never lies before c_s
     uint32_t fm1 = e >> 16;
@@ -609,7 +613,7 @@ __device__ __forceinline__ bool decode_span_impl(const DecObj &o, uint32_t slice
 #define CG_STEP(K)                                                                                          \
     {                                                                                                       \
         const uint32_t e0 = lds_u16(T.coarse_s + __byte_perm(x, 0, 0x4441) * (kLanes * 2u));                \
-        uint32_t s = (e0 + (x & 0xFFu)) >> 8;                                                               \
+        uint32_t s = __byte_perm(e0 + x, 0, 0x4441);                                                        \
         uint32_t e = lds_u32(T.tab_s + s * (kLanes * 4u));                                                  \
         float dq = lds_f32(T.dq_s + s * 4u);                                                                \
         uint32_t r = (x - e) & 0xFFFFu, fm1 = e >> 16;                                                      \
