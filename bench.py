@@ -54,7 +54,7 @@ E2E_LAYER_BATCHES = 8
 # DRAM bytes (read + write) of one k_decode_all launch on the full Llama-70B
 # workload: ncu capture of the first 8 layers (600.4 MB, grows with layers)
 # scaled by 80/8.  Must be reset to None whenever k_decode_all changes.
-DECODE_TRAFFIC_BYTES = 600.4e6 * 10
+DECODE_TRAFFIC_BYTES = 600.0e6 * 10
 
 
 def peaks():
