@@ -709,7 +709,9 @@ __device__ bool decode_span(const DecObj &o, uint32_t slice, uint32_t grp, uint3
     }
 #define CG_SPAN(E, GG, CC) \
     decode_span_impl<E, GG, CC, Out, kW>(o, slice, grp, sp, step, S, R, O, status, sb, se, eb, ee, nsteps)
+    // compile-time row strides for the two common widths: 8 and 32 heads of 128
     if (g.G == 10 && g.C == 1024) return ee != eb ? CG_SPAN(true, 10, 1024) : CG_SPAN(false, 10, 1024);
+    if (g.G == 10 && g.C == 4096) return ee != eb ? CG_SPAN(true, 10, 4096) : CG_SPAN(false, 10, 4096);
     if (g.G == 10) return ee != eb ? CG_SPAN(true, 10, 0) : CG_SPAN(false, 10, 0);
     return ee != eb ? CG_SPAN(true, 0, 0) : CG_SPAN(false, 0, 0);
 #undef CG_SPAN

@@ -988,6 +988,7 @@ static cudaError_t launch_stats(dim3 grid, cudaStream_t s, const EncArgs &a, con
     auto k = NL > 1                ? k_stats<NL, 0, false>
              : lv.raw_delta        ? (a.g.C == 1024 ? k_stats<1, 1024, true> : k_stats<1, 0, true>)
              : a.g.C == 1024       ? k_stats<1, 1024, false>
+             : a.g.C == 4096       ? k_stats<1, 4096, false>
                                    : k_stats<1, 0, false>;
     // per device, so set before every launch (a host-side call)
     const cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -1130,7 +1131,11 @@ static cg_status encode_levels(const cg_config *cfg, uint32_t levels, const floa
                     : levels == 3 ? launch_stats<3>(grid, s, a0, st, lv)
                                   : launch_stats<4>(grid, s, a0, st, lv);
     CG_CUDA_TRY(e);
-    auto k_enc = g.G == 10 && g.C == 1024 ? k_encode<10, 1024> : g.G == 10 ? k_encode<10, 0> : k_encode<0, 0>;
+    // compile-time row strides for the two common widths: 8 and 32 heads of 128
+    auto k_enc = g.G == 10 && g.C == 1024   ? k_encode<10, 1024>
+                 : g.G == 10 && g.C == 4096 ? k_encode<10, 4096>
+                 : g.G == 10                ? k_encode<10, 0>
+                                            : k_encode<0, 0>;
     CG_CUDA_TRY(cudaFuncSetAttribute(k_enc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEncSmemBytes));
     const uint32_t enc_warps = (uint32_t)(g.spans_total < (uint64_t)kMaxEncWarps ? g.spans_total : kMaxEncWarps);
     const uint64_t fixed = bd.anchors_bytes + bd.scales_bytes + bd.table_off_bytes + bd.stream_off_bytes +
