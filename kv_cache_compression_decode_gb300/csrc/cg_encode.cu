@@ -985,7 +985,7 @@ template <uint32_t NL>
 static cudaError_t launch_stats(dim3 grid, cudaStream_t s, const EncArgs &a, const StepTable &st, const StatsLevels &lv) {
     constexpr int bytes = (int)stats_smem_bytes<NL>();
     // the raw counts (grouping ablation) only come with one level
-    auto k = NL > 1                ? k_stats<NL, 0, false>
+    auto k = NL > 1                ? (a.g.C == 1024 ? k_stats<NL, 1024, false> : k_stats<NL, 0, false>)
              : lv.raw_delta        ? (a.g.C == 1024 ? k_stats<1, 1024, true> : k_stats<1, 0, true>)
              : a.g.C == 1024       ? k_stats<1, 1024, false>
              : a.g.C == 4096       ? k_stats<1, 4096, false>
