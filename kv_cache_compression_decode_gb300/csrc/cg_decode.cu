@@ -502,15 +502,20 @@ struct PagedDst {
 
 // Paged layout: token t lives in block table[t >> bshift], row t & mask.
 // A group (at most G <= block_tokens rows) touches at most two blocks, whose
-// bases are looked up when the group starts.  A physical block outside the
-// pool stops the span (ok() turns false) before anything is written there.
+// bases are looked up when the group starts: rows k < kb of the group lie in
+// token t's block at r0 + k * stride, the rest in the next block at q1 + k *
+// stride (q1 = that block's row 0 less kb rows).  kTsC: the token stride is
+// the row length C, a compile-time constant where C is, so a row's offset is
+// too.  A physical block outside the pool stops the span (ok() turns false)
+// before anything is written there.
+template <bool kTsC>
 struct PagedOut {
     uint16_t *slice;  // pool + layer and K/V offsets + lane's channel
     const uint32_t *table;
     uint32_t n_blocks, n_pool, bshift;
     uint64_t block_stride, ts;
-    uint32_t t;
-    uint16_t *b0, *b1;
+    uint32_t t, kb;
+    uintptr_t r0, q1;
     bool good;
     __device__ __forceinline__ uint16_t *block(uint32_t lb) {
         if (lb >= n_blocks) return slice;  // past the last token: never a row's block
@@ -521,16 +526,19 @@ struct PagedOut {
         }
         return slice + (uint64_t)pb * block_stride;
     }
-    __device__ __forceinline__ void seek(uint32_t tok, uint32_t = 0) {
+    __device__ __forceinline__ void seek(uint32_t tok, uint32_t C) {
+        const uint64_t stride = kTsC ? C : ts;
+        const uint32_t lb = tok >> bshift, off = tok & ((1u << bshift) - 1u);
         t = tok;
-        b0 = block(t >> bshift);
-        b1 = block((t >> bshift) + 1u);
+        kb = (1u << bshift) - off;
+        r0 = reinterpret_cast<uintptr_t>(block(lb)) + (uint64_t)off * stride * 2u;
+        q1 = reinterpret_cast<uintptr_t>(block(lb + 1u)) - (uint64_t)kb * stride * 2u;
     }
-    __device__ __forceinline__ uint16_t *row(uint32_t k, uint32_t = 0) const {
-        const uint32_t u = t + k;
-        return ((u >> bshift) != (t >> bshift) ? b1 : b0) + (uint64_t)(u & ((1u << bshift) - 1u)) * ts;
+    __device__ __forceinline__ uint16_t *row(uint32_t k, uint32_t C) const {
+        const uint64_t stride = kTsC ? C : ts;
+        return reinterpret_cast<uint16_t *>((k < kb ? r0 : q1) + (uint64_t)k * stride * 2u);
     }
-    __device__ __forceinline__ void advance(uint32_t n, uint32_t = 0) { seek(t + n); }
+    __device__ __forceinline__ void advance(uint32_t n, uint32_t C) { seek(t + n, C); }
     __device__ __forceinline__ bool ok() const { return good; }
 };
 
@@ -733,9 +741,10 @@ __device__ __forceinline__ Ring make_ring(const Shm &S) {
     return R;
 }
 
-// kPaged: rows go to the blocks of `pd`, else to out[L][2][T][C].  kW: the
+// kPaged: rows go to the blocks of `pd` (kTsC: its token stride is C), else
+// to out[L][2][T][C].  kW: the
 // time-out test kernel (a withheld ring segment, short waits).
-template <bool kPaged, bool kW = false>
+template <bool kPaged, bool kW = false, bool kTsC = false>
 __global__ void __maxnreg__(kDecRegs) k_decode_all(DecObj o, StepTable st, uint16_t *out, PagedDst pd,
                                                    uint32_t *status) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -752,7 +761,7 @@ __global__ void __maxnreg__(kDecRegs) k_decode_all(DecObj o, StepTable st, uint1
     for (uint64_t sp = warp; sp < o.g.spans_total; sp += nw) {
         bool alive;
         if (kPaged) {
-            PagedOut O;
+            PagedOut<kTsC> O;
             O.slice = pd.pool + (uint64_t)(slice >> 1) * pd.layer_stride + (uint64_t)(slice & 1u) * pd.kv_stride + c;
             O.table = pd.table;
             O.n_blocks = pd.n_blocks;
@@ -761,7 +770,7 @@ __global__ void __maxnreg__(kDecRegs) k_decode_all(DecObj o, StepTable st, uint1
             O.block_stride = pd.block_stride;
             O.ts = pd.token_stride;
             O.good = true;
-            alive = decode_span<PagedOut, kW>(o, slice, grp, (uint32_t)sp, step, S, R, O, status);
+            alive = decode_span<PagedOut<kTsC>, kW>(o, slice, grp, (uint32_t)sp, step, S, R, O, status);
         } else {
             const LinearOut<false> O{out + (uint64_t)slice * o.g.T * o.g.C, 0, c, nullptr};
             alive = decode_span<LinearOut<false>, kW>(o, slice, grp, (uint32_t)sp, step, S, R, O, status);
@@ -801,6 +810,9 @@ static cudaError_t set_smem_attrs() {
                                          (int)dec_smem_bytes(kMaxDecWarps));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_decode_all<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)dec_smem_bytes(kMaxDecWarps));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_decode_all<true, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)dec_smem_bytes(kMaxDecWarps));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_decode_jobs, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -959,8 +971,9 @@ extern "C" cg_status cg_decode_paged(const cg_config *cfg, const cg_encoded *enc
     const dim3 grid(o.g.NG, o.g.n_slices);
     CG_CUDA_TRY(set_smem_attrs());
     const uint32_t nwarps = warps_for(o.g.spans_total);
-    k_decode_all<true><<<grid, nwarps * 32, dec_smem_bytes(nwarps), static_cast<cudaStream_t>(stream)>>>(
-        o, st, nullptr, pd, dev_status);
+    auto k = pd.token_stride == o.g.C ? k_decode_all<true, false, true> : k_decode_all<true>;
+    k<<<grid, nwarps * 32, dec_smem_bytes(nwarps), static_cast<cudaStream_t>(stream)>>>(o, st, nullptr, pd,
+                                                                                         dev_status);
     CG_CUDA_TRY(cudaGetLastError());
     return CG_OK;
 }

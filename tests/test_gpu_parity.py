@@ -320,16 +320,21 @@ def test_full_size_mistral7b_mixed_levels():
 
 
 def _paged(layout, L, npool, bt, Cc):
-    """Pool shape and (layer, K/V, block, token) strides of two paged layouts."""
+    """Pool shape and (layer, K/V, block, token) strides of three paged layouts."""
     if layout == "layer_major":  # [L][n_pool][2][bt][C]
         return (L, npool, 2, bt, Cc), dict(layer_stride=npool * 2 * bt * Cc, block_stride=2 * bt * Cc,
                                            kv_stride=bt * Cc, token_stride=Cc)
+    if layout == "padded":  # [L][n_pool][2][bt][C + 64]: token rows longer than C
+        W = Cc + 64
+        return (L, npool, 2, bt, W), dict(layer_stride=npool * 2 * bt * W, block_stride=2 * bt * W,
+                                          kv_stride=bt * W, token_stride=W)
     return (npool, L, 2, bt, Cc), dict(layer_stride=2 * bt * Cc, block_stride=L * 2 * bt * Cc,  # [n_pool][L][2][bt][C]
                                        kv_stride=bt * Cc, token_stride=Cc)
 
 
 @needs_gpu
-@pytest.mark.parametrize("layout,bt", [("layer_major", 16), ("block_major", 32), ("layer_major", 1024)])
+@pytest.mark.parametrize("layout,bt", [("layer_major", 16), ("block_major", 32), ("layer_major", 1024),
+                                       ("padded", 16)])
 def test_paged_decode_matches_oracle(layout, bt):
     """Decode straight into a paged block pool through a shuffled block table:
     gathering the blocks back gives the oracle's cache bit for bit, and the
@@ -351,10 +356,11 @@ def test_paged_decode_matches_oracle(layout, bt):
     torch.cuda.synchronize()
     assert C.read_status(status) == C.CG_OK
     P16 = pool.cpu().numpy().view(np.uint16)
-    blk = (lambda pb: P16[:, pb]) if layout == "layer_major" else (lambda pb: P16[pb])
-    got = np.concatenate([blk(pb) for pb in perm], axis=2)  # [L][2][nb * bt][C]
-    assert np.array_equal(got[:, :, :T], odec)
+    blk = (lambda pb: P16[:, pb]) if layout != "block_major" else (lambda pb: P16[pb])
+    got = np.concatenate([blk(pb) for pb in perm], axis=2)  # [L][2][nb * bt][row length]
+    assert np.array_equal(got[:, :, :T, :Cc], odec)
     assert (got[:, :, T:] == 0xFFFF).all()
+    assert (got[..., Cc:] == 0xFFFF).all()  # a padded row's tail
     for pb in sorted(set(range(npool)) - set(perm.tolist())):
         assert (blk(pb) == 0xFFFF).all()
 
