@@ -135,9 +135,9 @@ class Workload:
 TINY = Workload("tiny-4L-256T-8x128", 4, 256, 1024, 0.95, 2, 0, 0, 1536)
 # Tokens per stream: a decode block serves one (layer, K/V, 32-channel group)
 # with one warp per stream, so the stream length sets the warps per block --
-# 12 for the 16384-token Llama-70B slices, 8 for the 4096-token Llama-7B
+# 12 for the 16384-token Llama-70B slices, 10 for the 4096-token Llama-7B
 # slices, 3 per 1536-token chunk for the chunked Mistral-7B cache.
-LLAMA7B = Workload("llama7b-mha-32L-4096T-32x128", 32, 4096, 4096, 0.95, 2, 0, 0, 512)
+LLAMA7B = Workload("llama7b-mha-32L-4096T-32x128", 32, 4096, 4096, 0.95, 2, 0, 0, 410)
 MISTRAL7B = Workload("mistral7b-gqa-32L-16384T-8x128-chunk1536", 32, 16384, 1024, 0.95, 2, 0, 1536, 512)
 LLAMA70B = Workload("llama70b-gqa-80L-16384T-8x128", 80, 16384, 1024, 0.9, 4, 0, 0, 1366)
 
