@@ -519,7 +519,7 @@ def main():
         del host_kv, bencs
 
     base = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:  # the oracle baseline belongs to the 1-GPU line
         base = cpu_baseline(w)
     # grouping ablation of the same cache (outside the timed region): ideal
     # bits/value with per-(layer, K/V, channel), per-(layer, K/V) and
