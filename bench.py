@@ -383,6 +383,9 @@ def main():
     ap.add_argument("--stream-slots", type=int, default=3, help="streamed: staging slots")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: use the first N layers of the workload (not a bench line)")
+    ap.add_argument("--cache", default="synthetic", choices=["synthetic", "zeros", "last-layers"],
+                    help="profiling only, with --layers: the workload's first layers, an all-zero cache of "
+                         "that size, or the workload's last layers")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -402,12 +405,20 @@ def main():
     torch.cuda.set_device(dev)
     base_w = synth.LLAMA70B if args.workload == "llama70b" else synth.LLAMA7B
     w = base_w
+    steps = C.layer_steps(base_w.L)
     if args.layers:
         import dataclasses
-        w = dataclasses.replace(w, name=f"{w.name}-first{args.layers}layers", L=args.layers)
-    cfg = C.Config(w.L, w.T, w.C, w.group_size, w.chunk, w.tokens_per_stream,
-                   C.layer_steps(base_w.L)[: w.L])
-    kv = w.generate(device=dev)
+        where = {"synthetic": "first", "zeros": "zero", "last-layers": "last"}[args.cache]
+        w = dataclasses.replace(w, name=f"{w.name}-{where}{args.layers}layers", L=args.layers)
+    if args.layers and args.cache == "last-layers":  # the whole cache drawn, its last layers kept
+        kv = base_w.generate(device=dev)[base_w.L - w.L:].contiguous()
+        steps = steps[base_w.L - w.L:]
+    elif args.layers and args.cache == "zeros":
+        kv = torch.zeros((w.L, 2, w.T, w.C), dtype=torch.float16, device=dev)
+    else:
+        kv = w.generate(device=dev)
+    cfg = C.Config(w.L, w.T, w.C, w.group_size, w.chunk, w.tokens_per_stream, steps[: w.L])
+    torch.cuda.empty_cache()
     enc = C.Encoder(cfg, dev)
     out = torch.empty_like(kv)
     dstatus = C.new_status(dev)
