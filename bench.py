@@ -159,24 +159,31 @@ def cpu_baseline(workload, seconds_hint=20.0):
                   O.layer_steps(workload.L)[:L1])
     x16 = x.view(np.uint16)
     t0 = time.perf_counter()
-    reps = 0
+    reps, t_enc, t_dec = 0, 0.0, 0.0
     while True:
+        ta = time.perf_counter()
         enc = O.encode(oc, x16, nthreads=cores)
+        tb = time.perf_counter()
         O.decode(oc, enc, nthreads=cores)
+        t_enc, t_dec = t_enc + (tb - ta), t_dec + (time.perf_counter() - tb)
         reps += 1
         if time.perf_counter() - t0 > min(seconds_hint, 30.0) or reps >= 5:
             break
-    dt = (time.perf_counter() - t0) / reps
-    gbs = x16.nbytes / dt / 1e9
+    gbs = x16.nbytes / ((t_enc + t_dec) / reps) / 1e9
     # one thread on the first layer (two slices), for the per-core figure
     oc1 = O.Config(1, workload.T, workload.C, 10, workload.chunk, workload.tokens_per_stream,
                    O.layer_steps(workload.L)[:1])
     x1 = np.ascontiguousarray(x16[:1])
-    t1 = time.perf_counter()
-    O.decode(oc1, O.encode(oc1, x1, nthreads=1), nthreads=1)
-    gbs1 = x1.nbytes / (time.perf_counter() - t1) / 1e9
+    ta = time.perf_counter()
+    enc1 = O.encode(oc1, x1, nthreads=1)
+    tb = time.perf_counter()
+    O.decode(oc1, enc1, nthreads=1)
+    tc = time.perf_counter()
+    gbs1 = x1.nbytes / (tc - ta) / 1e9
     return {"value": gbs, "unit": UNIT, "cores": min(cores, 2 * L1), "host_cores": cores, "kind": "oracle",
-            "single_thread_value": gbs1,
+            "encode_value": x16.nbytes / (t_enc / reps) / 1e9, "decode_value": x16.nbytes / (t_dec / reps) / 1e9,
+            "single_thread_value": gbs1, "single_thread_encode_value": x1.nbytes / (tb - ta) / 1e9,
+            "single_thread_decode_value": x1.nbytes / (tc - tb) / 1e9,
             "sample": f"encode+decode of layers 0..{L1 - 1} ({2 * L1} slices of {workload.T} tokens x "
                       f"{workload.C} channels, {x16.nbytes / 1e6:.0f} MB fp16) of {workload.name}, {reps} reps, "
                       f"one thread per (layer, K/V) slice; single_thread_value: layer 0 on one thread"}
